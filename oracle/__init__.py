@@ -1,0 +1,165 @@
+"""fp64 CPU oracle for the exact attention forward pass.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may import this package. It
+shares no code with the CUDA path and nothing in the product path calls it.
+
+``oracle.c`` holds the arithmetic (the materialising two-pass definition, the
+two online forms and the split-KV combine, each citing its passage);
+``numpy_ref.py`` is an independent vectorised restatement of the definition
+used only to cross-check the C code on small inputs. This file only marshals
+arguments through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        # ORACLE_LIB lets the mutation tests load a copy of the oracle with a
+        # planted mistake; nothing else sets it.
+        path = os.environ.get("ORACLE_LIB") or _build.build()
+        L = ctypes.CDLL(path)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        dblp = ctypes.POINTER(ctypes.c_double)
+        i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        common = [u16p, u16p, u16p, i64, i64, i64, i64, i64, i32, f32]
+        L.oracle_attention_rows.argtypes = common + [i64p, i64, dblp, dblp, i32]
+        L.oracle_attention.argtypes = common + [dblp, dblp, i32]
+        L.oracle_probs_row.argtypes = [u16p, u16p, i64, i64, i64, i64, i64, i32, f32,
+                                       i64, i64, i64, dblp]
+        L.oracle_online_rows.argtypes = common + [i64, i32, i64p, i64, dblp, dblp, i32]
+        L.oracle_split_rows.argtypes = common + [i64p, i64, i64p, i64, dblp, dblp, i32]
+        L.oracle_max_threads.argtypes = []
+        for f in (L.oracle_attention_rows, L.oracle_attention, L.oracle_probs_row,
+                  L.oracle_online_rows, L.oracle_split_rows, L.oracle_max_threads):
+            f.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 CPU tensor -> contiguous uint16 array of its bit patterns."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"oracle inputs are bf16, got {t.dtype}")
+    t = t.detach().to("cpu").contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _dims(q, k, v):
+    if q.dim() != 4 or k.shape != v.shape or k.dim() != 4:
+        raise ValueError("expected q [B,H,Sq,d] and k, v [B,H,Sk,d]")
+    B, H, Sq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("q and k/v disagree on B, H or d")
+    return B, H, Sq, k.shape[2], d
+
+
+def _rows_array(rows, B, H, Sq):
+    if rows is None:
+        return None
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    return r
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
+
+
+def attention(q, k, v, causal: bool, scale: float, rows=None, threads: int = 0):
+    """Definition of attention in fp64.
+
+    rows=None: returns (o [B,H,Sq,d], lse [B,H,Sq]) float64 arrays.
+    rows=[(b,h,i), ...]: returns (o [n,d], lse [n]) for those rows.
+    """
+    B, H, Sq, Sk, d = _dims(q, k, v)
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    L = lib()
+    args = (_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
+            B, H, Sq, Sk, d, int(bool(causal)), ctypes.c_float(scale))
+    if rows is None:
+        o = np.empty((B, H, Sq, d), dtype=np.float64)
+        lse = np.empty((B, H, Sq), dtype=np.float64)
+        _check(L.oracle_attention(*args, _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                  int(threads)), "attention")
+        return o, lse
+    r = _rows_array(rows, B, H, Sq)
+    n = r.shape[0]
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _check(L.oracle_attention_rows(*args, _ptr(r, ctypes.c_int64), n, _ptr(o, ctypes.c_double),
+                                   _ptr(lse, ctypes.c_double), int(threads)), "attention_rows")
+    return o, lse
+
+
+def probs_row(q, k, causal: bool, scale: float, b: int, h: int, i: int):
+    """Softmax row P_i over all Sk keys (hidden keys 0), fp64."""
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    qb, kb = _bits(q), _bits(k)
+    p = np.empty((Sk,), dtype=np.float64)
+    _check(lib().oracle_probs_row(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), B, H, Sq,
+                                  Sk, d, int(bool(causal)), ctypes.c_float(scale), b, h, i,
+                                  _ptr(p, ctypes.c_double)), "probs_row")
+    return p
+
+
+def _all_rows(B, H, Sq):
+    return [(b, h, i) for b in range(B) for h in range(H) for i in range(Sq)]
+
+
+def online(q, k, v, causal: bool, scale: float, block: int, form: int, rows=None, threads=0):
+    """Online (block-wise, one-pass) softmax forms; form 1 = page 1, form 2 = page 2 Ch. 3."""
+    B, H, Sq, Sk, d = _dims(q, k, v)
+    r = _rows_array(rows if rows is not None else _all_rows(B, H, Sq), B, H, Sq)
+    n = r.shape[0]
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _check(lib().oracle_online_rows(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                    _ptr(vb, ctypes.c_uint16), B, H, Sq, Sk, d,
+                                    int(bool(causal)), ctypes.c_float(scale), int(block), int(form),
+                                    _ptr(r, ctypes.c_int64), n, _ptr(o, ctypes.c_double),
+                                    _ptr(lse, ctypes.c_double), int(threads)), "online_rows")
+    return o, lse
+
+
+def split(q, k, v, causal: bool, scale: float, bounds, rows=None, threads=0):
+    """Split-KV partials over key chunks cut at ``bounds`` plus the final LSE combine."""
+    B, H, Sq, Sk, d = _dims(q, k, v)
+    r = _rows_array(rows if rows is not None else _all_rows(B, H, Sq), B, H, Sq)
+    n = r.shape[0]
+    bnd = np.ascontiguousarray(np.asarray(bounds, dtype=np.int64))
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _check(lib().oracle_split_rows(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                   _ptr(vb, ctypes.c_uint16), B, H, Sq, Sk, d, int(bool(causal)),
+                                   ctypes.c_float(scale), _ptr(bnd, ctypes.c_int64),
+                                   len(bnd) - 1, _ptr(r, ctypes.c_int64), n,
+                                   _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                   int(threads)), "split_rows")
+    return o, lse
+
+
+__all__ = ["attention", "probs_row", "online", "split", "max_threads", "lib"]
