@@ -1,0 +1,422 @@
+"""Benchmark: causal attention forward at B=4, H=32, S=8192, d=128 (bf16) on GB300.
+
+One step = one call of the attention forward over the whole batch (one launch
+of the tiled prefill kernel). Prints ONE JSON line on rank 0.
+
+  value     algorithmic TFLOP/s (4*d per visible (query, key) pair), inputs
+            resident in HBM, CUDA events on the launching stream, max over ranks
+  e2e       same metric through the public call with pinned host buffers:
+            H2D of Q, K, V + the call + D2H of O, LSE inside the timed region
+  roofline  achieved / measured bf16 tensor peak for the prefill kernel
+  verify    the decode-shaped split-KV path (B=16, H=32, Sq=5, Sk=4096) against
+            the measured HBM bandwidth
+  cpu_baseline  the fp64 oracle on a bounded sample of rows, host cores
+
+--impl reference times the fp64 CPU oracle instead (the only reference arm
+this method has) on the same workload, metric and unit.
+Multi-GPU (torchrun): every rank runs its own independent batch (weak
+scaling, no collective on the data path); value = all ranks' FLOPs / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_tiled_attention_03_gb300.inputs import HEADLINE, VERIFY, WORKLOADS, make_qkv, sample_rows, with_seed  # noqa: E402
+
+METRIC = "causal attn fwd TFLOP/s (bf16, B=4,H=32,S=8192,d=128) and % of GB300 BF16 peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+# ---------------------------------------------------------------- distributed helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max over ranks (the job is as slow as its slowest rank)."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_workload(name: str, rank: int):
+    """Each rank's own independent problem: same shape, seed offset by rank."""
+    w = WORKLOADS[name]
+    return with_seed(w, w.seed + 1000 * rank) if rank else w
+
+
+# ---------------------------------------------------------------- measurement helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+PREFILL_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_prefill_sm103.cu",
+                   "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
+VERIFY_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_verify.cu",
+                  "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
+
+
+def ncu_traffic(kernel: str, sources, units_per_launch: float):
+    """DRAM bytes per launch from the committed ncu summary, scaled to this
+    launch by the units processed; None if the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("source_sha") != source_hash(sources):
+        return None
+    return d["dram_bytes"] * units_per_launch / d["units"]
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            if t0 <= ts <= t1 + 0.15:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def time_steps(fn, steps, stream):
+    """Device time of `steps` back-to-back calls (CUDA events on `stream`)."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+def oracle_rows_flops(w, rows):
+    return sum(4 * w.d * w.visible_keys(i) for _, _, i in rows)
+
+
+def time_oracle_sample(w, q, k, v, budget_s: float, seed: int = 7):
+    """Time the oracle (as it stands) on a seeded sample of rows sized to ~budget_s."""
+    import oracle
+
+    probe = sample_rows(w, n_total=16, seed=seed)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.causal, w.scale, rows=probe)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    per_flop = dt / oracle_rows_flops(w, probe)
+    avg_row = w.exact_flops() / (w.B * w.H * w.Sq)
+    n = int(max(16, min(w.B * w.H * w.Sq, budget_s / (per_flop * avg_row))))
+    rows = sample_rows(w, n_total=n, seed=seed + 1)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.causal, w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    return rows, dt, oracle_rows_flops(w, rows)
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the fp64 CPU oracle on the same workload, rank 0 only."""
+    if rank != 0:
+        return 0
+    import oracle
+
+    w = WORKLOADS[args.workload]
+    q, k, v = make_qkv(w)
+    cores = oracle.max_threads()
+    total_budget = 120.0
+    rows_probe, dt_probe, fl_probe = time_oracle_sample(w, q, k, v, budget_s=2.0)
+    per_flop = dt_probe / fl_probe
+    avg_row = w.exact_flops() / (w.B * w.H * w.Sq)
+    n_rows = int(max(1, total_budget / (args.steps + args.warmup) / (per_flop * avg_row)))
+    times, flops = [], []
+    for s in range(args.warmup + args.steps):
+        rows = sample_rows(w, n_total=n_rows, seed=100 + s)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, w.causal, w.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            flops.append(oracle_rows_flops(w, rows))
+    value = sum(flops) / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(w, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_rows} seeded query rows of the workload per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(w, world):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
+            "causal": w.causal, "scale": w.scale, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (no flush needed)",
+            "flops_per_step": w.exact_flops(),
+            "score_matrix_bytes_avoided": w.score_matrix_bytes()}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import exact_tiled_attention_03_gb300 as fa
+    from exact_tiled_attention_03_gb300 import _capi
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    peaks = load_peaks()
+    fa.load()
+
+    w = rank_workload(args.workload, rank)
+    q_h, k_h, v_h = make_qkv(w)
+    q, k, v = q_h.to(device), k_h.to(device), v_h.to(device)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    sptr = stream.cuda_stream
+
+    def step():
+        st = _capi.fa_forward(q, k, v, o, lse, w.B, w.H, w.Sq, w.Sk, w.d, w.causal, w.scale, sptr)
+        if st != 0:
+            raise _capi.FAError(st, "fa_forward")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    fa.check(fa.fa_device_status(sptr), "device status after warm-up")
+
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = clk.mark()
+        dt = time_steps(step, args.steps, stream)
+        t1 = clk.mark()
+        barrier(world)
+    fa.check(fa.fa_device_status(sptr), "device status after timed region")
+    dt_max = reduce_max(dt, world, device)
+    flops_all = reduce_sum(float(w.exact_flops() * args.steps), world, device)
+    value = flops_all / dt_max / 1e12
+    per_launch_s = dt / args.steps
+    achieved = w.exact_flops() / per_launch_s / 1e12
+    clocks = clk.summary(t0, t1)
+
+    # end to end through the public call, pinned host buffers, copies timed
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True)
+            step()
+            op.copy_(o, non_blocking=True)
+            lp.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        n_e2e = max(3, min(20, args.steps // 10))
+        barrier(world)
+        de = time_steps(e2e_step, n_e2e, stream)
+        de = reduce_max(de, world, device)
+        e2e = {"value": reduce_sum(float(w.exact_flops() * n_e2e), world, device) / de / 1e12,
+               "unit": "TFLOP/s", "steps": n_e2e,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q, k, v)),
+               "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size()}
+
+    # the decode-shaped verify path, against the HBM roofline
+    verify = None
+    if not args.no_verify:
+        wv = rank_workload(VERIFY, rank)
+        qv, kv_, vv = (t.to(device) for t in make_qkv(wv))
+        ov = torch.empty_like(qv)
+        lv = torch.empty((wv.B, wv.H, wv.Sq), dtype=torch.float32, device=device)
+        n_split = _capi.fa_verify_auto_splits(wv.B, wv.H, wv.Sq, wv.Sk, wv.d)
+        need = _capi.fa_verify_workspace_size(wv.B, wv.H, wv.Sq, wv.Sk, wv.d, n_split)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+
+        def vstep():
+            st = _capi.fa_verify_forward(qv, kv_, vv, ov, lv, wv.B, wv.H, wv.Sq, wv.Sk, wv.d,
+                                         wv.causal, wv.scale, n_split, ws, need, sptr)
+            if st != 0:
+                raise _capi.FAError(st, "fa_verify_forward")
+
+        for _ in range(args.warmup):
+            vstep()
+        n_v = max(10, args.steps)
+        dv = time_steps(vstep, n_v, stream)
+        fa.check(fa.fa_device_status(sptr), "device status after verify")
+        per = dv / n_v
+        gbs = wv.io_bytes() / per / 1e9
+        verify = {"workload": wv.name, "us_per_step": per * 1e6, "GB/s": gbs,
+                  "hbm_peak_GB/s": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+                  "bytes_per_step": wv.io_bytes(), "n_split": n_split,
+                  "launches_per_step": 1 if n_split == 1 else 2,
+                  "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, 1.0)}
+        del qv, kv_, vv, ov, lv, ws
+
+    # the CPU oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+
+        rows, dtc, flc = time_oracle_sample(w, q_h, k_h, v_h, budget_s=args.cpu_budget)
+        cpu = {"value": flc / dtc / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"{len(rows)} seeded query rows of {w.name} "
+                         f"({flc:.3e} algorithmic FLOPs, {dtc:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_block(w, world),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "peak_source": f"{peaks['source']} bf16 burst",
+                         "kernel": "fa_prefill_kernel<128>",
+                         "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, 1.0)},
+            "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
+            "e2e": e2e, "verify": verify, "cpu_baseline": cpu, "clocks": clocks,
+            "gpu_launches": args.steps,
+            "gpu": torch.cuda.get_device_name(device),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-verify", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,45 @@
-"""GB300-native exact FlashAttention forward (sm_103a CUDA behind a C ABI)."""
+"""GB300-native exact attention forward (sm_103a CUDA behind a C ABI).
+
+The kernels live in ``lib/libfa_gb300.so`` (built from ``csrc/`` by
+``build.py``); ``_capi`` binds the C entry points by name. ``attention``
+is the convenience call: it allocates O and LSE with torch (device memory
+is the only thing torch provides here) and runs ``fa_forward`` on the
+current stream.
+"""
+from __future__ import annotations
+
+from ._capi import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED,
+                    FA_ERR_WORKSPACE, FA_OK, FA_VERIFY_MAX_SQ, FAError, check, fa_device_status,
+                    fa_forward, fa_forward_ws, fa_prefill_forward, fa_status_string,
+                    fa_verify_auto_splits, fa_verify_forward, fa_verify_workspace_size,
+                    fa_workspace_size, load)
+
+__all__ = [
+    "attention", "fa_forward", "fa_forward_ws", "fa_prefill_forward", "fa_verify_forward",
+    "fa_workspace_size", "fa_verify_workspace_size", "fa_verify_auto_splits", "fa_status_string",
+    "fa_device_status", "FAError", "check", "load", "FA_OK", "FA_ERR_INVALID_ARG",
+    "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE", "FA_VERIFY_MAX_SQ",
+]
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """O, LSE = attention(Q, K, V) for contiguous bf16 CUDA tensors [B, H, S, d].
+
+    Returns O (bf16, like q) and LSE (fp32 [B, H, Sq]). Raises FAError on a
+    non-OK status.
+    """
+    import math
+
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor [B, H, S, d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    check(fa_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream), "fa_forward")
+    return o, lse

@@ -1,0 +1,157 @@
+"""ctypes binding of the C ABI in include/fa.h and include/fa_testing.h.
+
+Argument marshalling only: every entry point keeps its C name and argument
+order; a torch tensor may stand wherever the C call takes a device pointer,
+and a torch.cuda.Stream (or None = torch's current stream) where it takes a
+stream. There is no fallback: if the CUDA library is missing the first call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_WORKSPACE = 5
+FA_VERIFY_MAX_SQ = 16
+
+# Every function the headers declare, with its ctypes signature.
+_P, _I64, _I32, _F32, _SZ, _U64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                                   ctypes.c_size_t, ctypes.c_uint64)
+_ATTN = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I32, _F32]
+SIGNATURES = {
+    "fa_forward": (_I32, _ATTN + [_P]),
+    "fa_workspace_size": (_SZ, [_I64] * 5),
+    "fa_forward_ws": (_I32, _ATTN + [_P, _SZ, _P]),
+    "fa_prefill_forward": (_I32, _ATTN + [_P]),
+    "fa_verify_forward": (_I32, _ATTN + [_I32, _P, _SZ, _P]),
+    "fa_verify_workspace_size": (_SZ, [_I64] * 5 + [_I32]),
+    "fa_verify_auto_splits": (_I32, [_I64] * 5),
+    "fa_status_string": (ctypes.c_char_p, [_I32]),
+    "fa_device_status": (_I32, [_P]),
+    "fa_reference_forward_simt": (_I32, _ATTN + [_P]),
+    "fa_selftest_umma": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
+    "fa_selftest_wait_timeout": (_I32, [_U64, _P]),
+}
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"the CUDA library {path} is missing; build it with "
+            "`python -m exact_tiled_attention_03_gb300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"expected a tensor, an int address or None, got {type(x).__name__}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def fa_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def fa_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream=None) -> int:
+    return load().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, d,
+                             int(bool(causal)), float(scale), _stream(stream))
+
+
+def fa_workspace_size(B, H, Sq, Sk, d) -> int:
+    return load().fa_workspace_size(B, H, Sq, Sk, d)
+
+
+def fa_forward_ws(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, workspace, ws_bytes,
+                  stream=None) -> int:
+    return load().fa_forward_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, d,
+                                int(bool(causal)), float(scale), _ptr(workspace), int(ws_bytes),
+                                _stream(stream))
+
+
+def fa_prefill_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream=None) -> int:
+    return load().fa_prefill_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk,
+                                     d, int(bool(causal)), float(scale), _stream(stream))
+
+
+def fa_verify_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, n_split, workspace,
+                      ws_bytes, stream=None) -> int:
+    return load().fa_verify_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk,
+                                    d, int(bool(causal)), float(scale), int(n_split),
+                                    _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def fa_verify_workspace_size(B, H, Sq, Sk, d, n_split) -> int:
+    return load().fa_verify_workspace_size(B, H, Sq, Sk, d, int(n_split))
+
+
+def fa_verify_auto_splits(B, H, Sq, Sk, d) -> int:
+    return load().fa_verify_auto_splits(B, H, Sq, Sk, d)
+
+
+def fa_device_status(stream=None) -> int:
+    return load().fa_device_status(_stream(stream))
+
+
+def fa_reference_forward_simt(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale,
+                              stream=None) -> int:
+    return load().fa_reference_forward_simt(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                            Sq, Sk, d, int(bool(causal)), float(scale),
+                                            _stream(stream))
+
+
+def fa_selftest_umma(a, b, c, n, k, b_mn_major, stream=None) -> int:
+    return load().fa_selftest_umma(_ptr(a), _ptr(b), _ptr(c), int(n), int(k), int(b_mn_major),
+                                   _stream(stream))
+
+
+def fa_selftest_wait_timeout(timeout_ns, stream=None) -> int:
+    return load().fa_selftest_wait_timeout(int(timeout_ns), _stream(stream))
+
+
+def check(status: int, what: str = "fa call"):
+    if status != FA_OK:
+        raise FAError(status, what)

@@ -1,0 +1,355 @@
+// fa_abi.cu — the C ABI declared in include/fa.h and include/fa_testing.h:
+// argument validation, shape dispatch (prefill vs split-KV), TMA descriptor
+// encoding, the device status word, and the stream-ordered workspace of
+// fa_forward. No compute happens here.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_testing.h"
+
+// Library-owned status word (one per device): kernels OR in a bit when a
+// bounded wait gives up; fa_device_status() reads and clears it.
+__device__ unsigned int g_fa_status_word;
+
+namespace fa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    unsigned int *status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts and the device address of the status word, looked up once
+// per device with that device current.
+const DeviceInfo *device_info()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (!di.ready) {
+        if (cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return nullptr;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_fa_status_word) != cudaSuccess)
+            return nullptr;
+        di.status = static_cast<unsigned int *>(addr);
+        di.ready = true;
+    }
+    return &di;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape and argument checks shared by every attention entry point.
+fa_status_t validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                     bool any_d)
+{
+    if (!q || !k || !v || !o || !lse)
+        return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || d <= 0)
+        return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale))
+        return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.0f))
+        return FA_ERR_UNSUPPORTED;
+    if (any_d ? (d > 128) : (d != 64 && d != 128))
+        return FA_ERR_UNSUPPORTED;
+    const int64_t lim31 = (int64_t(1) << 31) - 1;
+    if (Sq > lim31 || Sk > lim31 || B > lim31 / H)
+        return FA_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    const int64_t lim62 = int64_t(1) << 62;
+    if (Sq > lim62 / (BH * d) || Sk > lim62 / (BH * d))
+        return FA_ERR_UNSUPPORTED;
+    if (!any_d && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)))
+        return FA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+// The kernels are built for sm_103a only.
+fa_status_t device_ok(const DeviceInfo **out)
+{
+    const DeviceInfo *di = device_info();
+    if (!di)
+        return FA_ERR_CUDA;
+    if (di->cc_major != 10 || di->cc_minor != 3)
+        return FA_ERR_UNSUPPORTED;
+    *out = di;
+    return FA_OK;
+}
+
+Problem make_problem(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                     int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal, float scale,
+                     void *stream, unsigned int *status)
+{
+    Problem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale = scale;
+    p.stream = static_cast<cudaStream_t>(stream);
+    p.status = status;
+    return p;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int verify_splits_or_auto(int n_split, int64_t BH, int64_t Sk, const DeviceInfo *di)
+{
+    return n_split > 0 ? n_split : verify_auto_splits(BH, Sk, di->num_sms);
+}
+
+}  // namespace
+
+bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                         uint64_t depth, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {inner, rows, depth};
+    const cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char *fa_status_string(fa_status_t s)
+{
+    switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape, alignment, scale or device";
+    case FA_ERR_CUDA: return "CUDA runtime or launch error";
+    case FA_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                               int causal, float scale, void *stream)
+{
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    return launch_prefill_sm103(
+        make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream, di->status));
+}
+
+size_t fa_verify_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                                int n_split)
+{
+    if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || d <= 0 || n_split < 0)
+        return 0;
+    if (n_split == 0) {
+        const DeviceInfo *di = device_info();
+        if (!di)
+            return 0;
+        n_split = verify_auto_splits(B * H, Sk, di->num_sms);
+    }
+    return verify_workspace_bytes(B * H, Sq, d, n_split);
+}
+
+int fa_verify_auto_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d)
+{
+    (void)Sq;
+    (void)d;
+    if (B <= 0 || H <= 0 || Sk <= 0)
+        return 0;
+    const DeviceInfo *di = device_info();
+    if (!di)
+        return 0;
+    return verify_auto_splits(B * H, Sk, di->num_sms);
+}
+
+fa_status_t fa_verify_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                              int causal, float scale, int n_split, void *workspace,
+                              size_t ws_bytes, void *stream)
+{
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    if (Sq > FA_VERIFY_MAX_SQ || B * H > 65535)
+        return FA_ERR_UNSUPPORTED;
+    const int64_t max_split = (Sk + kVerifyStageKeys - 1) / kVerifyStageKeys;
+    if (n_split < 0 || n_split > max_split || n_split > 65535)
+        return FA_ERR_INVALID_ARG;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    const int ns = verify_splits_or_auto(n_split, B * H, Sk, di);
+    const size_t need = verify_workspace_bytes(B * H, Sq, d, ns);
+    if (need > 0 && (!workspace || ws_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return FA_ERR_WORKSPACE;
+    return launch_verify(
+        make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream, di->status), ns,
+        workspace, ws_bytes);
+}
+
+size_t fa_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d)
+{
+    if (Sq > FA_VERIFY_MAX_SQ)
+        return 0;
+    return fa_verify_workspace_size(B, H, Sq, Sk, d, 0);
+}
+
+fa_status_t fa_forward_ws(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                          float scale, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (Sq > 0 && Sq <= FA_VERIFY_MAX_SQ)
+        return fa_verify_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, 0, workspace,
+                                 ws_bytes, stream);
+    return fa_prefill_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream);
+}
+
+fa_status_t fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                       float scale, void *stream)
+{
+    if (!(Sq > 0 && Sq <= FA_VERIFY_MAX_SQ))
+        return fa_prefill_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream);
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    if (B * H > 65535)
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    const int ns = verify_auto_splits(B * H, Sk, di->num_sms);
+    const size_t need = verify_workspace_bytes(B * H, Sq, d, ns);
+    void *ws = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    st = launch_verify(make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream,
+                                    di->status),
+                       ns, ws, need);
+    if (ws && cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK)
+        st = FA_ERR_CUDA;
+    return st;
+}
+
+fa_status_t fa_device_status(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    const DeviceInfo *di = device_info();
+    if (!di)
+        return FA_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, di->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(di->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return (word & kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status_t fa_reference_forward_simt(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                      int64_t d, int causal, float scale, void *stream)
+{
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, true);
+    if (st != FA_OK)
+        return st;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 1u)
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    return launch_reference_simt(
+        make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream, di->status));
+}
+
+fa_status_t fa_selftest_umma(const void *a, const void *b, float *c, int n, int k, int b_mn_major,
+                             void *stream)
+{
+    if (!a || !b || !c)
+        return FA_ERR_INVALID_ARG;
+    if ((n != 64 && n != 128) || (k != 64 && k != 128) || (b_mn_major != 0 && b_mn_major != 1))
+        return FA_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c))
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_umma(a, b, c, n, k, b_mn_major, static_cast<cudaStream_t>(stream),
+                                di->status);
+}
+
+fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
+{
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull)
+        return FA_ERR_INVALID_ARG;
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_wait(timeout_ns, static_cast<cudaStream_t>(stream), di->status);
+}
+
+}  // extern "C"

@@ -1,0 +1,493 @@
+// fa_prefill_sm103.cu — tiled exact attention forward on sm_103a tensor cores.
+//
+// The method is the FlashAttention forward of "Warmup Guide — Inference
+// Optimization at Depth", Chapter 4 and "FlashAttention, speculative
+// decoding, quantisation and parallelism", Mechanics: each block of query
+// rows stays on chip, K/V blocks stream through, S = Q K^T * scale is formed
+// one tile at a time, the online softmax of Chapter 3 keeps a running max m
+// and sum l and rescales the unnormalised accumulator by exp(m_old - m_new),
+// key blocks above the causal diagonal are skipped and the diagonal ones
+// masked, and O / l is written once together with the per-row statistics
+// (LSE = m + ln l).
+//
+// The GB300 shape of it (not the pages' SRAM/Hopper design):
+//   * one CTA per SM owns two 128-row query tiles of one (batch, head);
+//     both share every K/V tile it loads;
+//   * warp 8 (producer) moves Q once and then K_j, V_j through a ring of
+//     shared-memory stages with TMA (128-byte swizzle), one mbarrier pair per
+//     stage;
+//   * warp 9 (one elected thread) issues tcgen05.mma: S_t = Q_t K_j^T into
+//     tensor memory (TMEM), then O_t += P_t V_j, with V read MN-major straight
+//     from its row-major tile; completion is signalled with tcgen05.commit;
+//   * warps 0-3 and 4-7 are one softmax warpgroup per query tile; thread r
+//     owns row r (TMEM lane r). It pulls its S row out of TMEM, masks,
+//     computes the row max and exp2 of the shifted, log2(e)-scaled logits,
+//     writes P (bf16) into a swizzled shared-memory tile for the next MMA,
+//     and rescales its O row in TMEM when the max moved. At the end it
+//     divides by l, writes the bf16 O row into shared memory for a TMA store
+//     and writes its LSE;
+//   * the two warpgroups run out of phase, so the tensor core works on one
+//     tile while the other tile's softmax runs.
+// Every wait is bounded; on expiry the CTA stops, drains what it has in
+// flight, frees its tensor memory and sets the device status word.
+#include <cmath>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace prefill {
+
+constexpr int kBlockM = 128;   // query rows per tile = TMEM lanes
+constexpr int kBlockN = 128;   // keys per K/V tile
+constexpr int kTiles = 2;      // query tiles per CTA
+constexpr int kThreads = 320;  // 2 softmax warpgroups + producer warp + MMA warp
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (16 KB)
+
+template <int D>
+struct Cfg {
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kTileBytes = kBlockM * D * 2;  // Q, K, V or O tile
+    static constexpr int kStages = (D == 128) ? 3 : 6;
+    static constexpr int kPBytes = kBlockM * kBlockN * 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kTiles * kTileBytes;
+    static constexpr int kOffP = kOffKV + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffP + kTiles * kPBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+    static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+    static_assert(kColO1 + D <= kTmemCols, "TMEM budget");
+};
+
+struct Params {
+    int Sq, Sk, BH, n_qblk;
+    int causal;
+    float scale;       // softmax scale
+    float scale_log2;  // scale * log2(e)
+    float *lse;
+    unsigned int *status;
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t s_full[kTiles];
+    uint64_t s_free[kTiles];
+    uint64_t p_full[kTiles];
+    uint64_t o_done[kTiles];
+    uint64_t drain;
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// Number of keys visible to query row i (bottom-right causal alignment).
+__device__ __forceinline__ int visible_keys(int i, int Sq, int Sk, int causal)
+{
+    if (!causal)
+        return Sk;
+    int n = i + (Sk - Sq) + 1;
+    return n < 0 ? 0 : (n > Sk ? Sk : n);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const Params p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms.
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t *sQ = smem + C::kOffQ;
+    uint8_t *sKV = smem + C::kOffKV;
+    uint8_t *sP = smem + C::kOffP;
+    Bars *bars = reinterpret_cast<Bars *>(smem + C::kOffBar);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    // Heaviest query blocks first: with the causal mask the last blocks of a
+    // sequence see the most keys.
+    const int bh = blockIdx.x % p.BH;
+    const int qblk = p.n_qblk - 1 - static_cast<int>(blockIdx.x / p.BH);
+
+    int q0[kTiles], n_kv[kTiles], mask_from[kTiles];
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        q0[t] = qblk * (kTiles * kBlockM) + t * kBlockM;
+        if (q0[t] < p.Sq) {
+            const int last = min(q0[t] + kBlockM - 1, p.Sq - 1);
+            n_kv[t] = (visible_keys(last, p.Sq, p.Sk, p.causal) + kBlockN - 1) / kBlockN;
+            mask_from[t] = visible_keys(q0[t], p.Sq, p.Sk, p.causal) / kBlockN;
+        } else {
+            n_kv[t] = 0;
+            mask_from[t] = 0;
+        }
+    }
+    const int n_kv_max = max(n_kv[0], n_kv[1]);
+    const bool any_tile = q0[0] < p.Sq;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->s_free[t], 4);
+            mbar_init(&bars->p_full[t], 4);
+            mbar_init(&bars->o_done[t], 1);
+        }
+        mbar_init(&bars->drain, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        bars->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    int *abort_flag = &bars->abort_flag;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && any_tile) {
+            const uint64_t pol_stream = l2_policy_evict_first();  // Q: read once
+            const uint64_t pol_keep = l2_policy_evict_last();     // K/V: re-read by other q-blocks
+            uint32_t q_bytes = 0;
+            for (int t = 0; t < kTiles; ++t)
+                if (q0[t] < p.Sq)
+                    q_bytes += C::kTileBytes;
+            mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+            for (int t = 0; t < kTiles; ++t)
+                if (q0[t] < p.Sq)
+                    for (int b = 0; b < C::kBoxes; ++b)
+                        tma_load_3d_hint(sQ + t * C::kTileBytes + b * kBoxBytes, &tm_q,
+                                         &bars->q_full, b * 64, q0[t], bh, pol_stream);
+            int it = 0;
+            bool ok = true;
+            for (int j = 0; j < n_kv_max && ok; ++j) {
+                for (int which = 0; which < 2 && ok; ++which, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t use = it / C::kStages;
+                    if (use > 0 &&
+                        !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
+                    const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
+                    for (int b = 0; b < C::kBoxes; ++b)
+                        tma_load_3d_hint(sKV + s * C::kTileBytes + b * kBoxBytes, tm,
+                                         &bars->kv_full[s], b * 64, j * kBlockN, bh, pol_keep);
+                }
+            }
+            // Drain: every load issued must have landed before the CTA exits.
+            mbar_wait_drain(&bars->q_full, 0, p.status);
+            for (int k = max(0, it - C::kStages); k < it; ++k)
+                mbar_wait_drain(&bars->kv_full[k % C::kStages], (k / C::kStages) & 1, p.status);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && any_tile && n_kv_max > 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
+            const uint32_t colS[kTiles] = {C::kColS0, C::kColS1};
+            const uint32_t colO[kTiles] = {C::kColO0, C::kColO1};
+            const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV), sP_a = smem_u32(sP);
+            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
+            tc_fence_after_sync();
+            int it = 0;
+            for (int j = 0; j < n_kv_max && ok; ++j) {
+                // S_t = Q_t K_j^T
+                const int sk = it % C::kStages;
+                ok = mbar_wait(&bars->kv_full[sk], (it / C::kStages) & 1, abort_flag, p.status);
+                ++it;
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                for (int t = 0; t < kTiles; ++t) {
+                    if (j >= n_kv[t])
+                        continue;
+                    if (j > 0) {
+                        ok = mbar_wait(&bars->s_free[t], (j - 1) & 1, abort_flag, p.status);
+                        if (!ok)
+                            break;
+                        tc_fence_after_sync();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+                        const uint64_t da =
+                            smem_desc_sw128(sQ_a + t * C::kTileBytes + koff, 16, 1024);
+                        const uint64_t db =
+                            smem_desc_sw128(sKV_a + sk * C::kTileBytes + koff, 16, 1024);
+                        umma_bf16_ss(tmem + colS[t], da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&bars->s_full[t]);
+                }
+                if (!ok)
+                    break;
+                umma_commit(&bars->kv_empty[sk]);
+                // O_t += P_t V_j
+                const int sv = it % C::kStages;
+                ok = mbar_wait(&bars->kv_full[sv], (it / C::kStages) & 1, abort_flag, p.status);
+                ++it;
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                for (int t = 0; t < kTiles; ++t) {
+                    if (j >= n_kv[t])
+                        continue;
+                    ok = mbar_wait(&bars->p_full[t], j & 1, abort_flag, p.status);
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        const uint64_t da = smem_desc_sw128(
+                            sP_a + t * C::kPBytes + (kk / 4) * kBoxBytes + (kk % 4) * 32, 16,
+                            1024);
+                        const uint64_t db = smem_desc_sw128(
+                            sKV_a + sv * C::kTileBytes + kk * 16 * 128, kBoxBytes, 1024);
+                        umma_bf16_ss(tmem + colO[t], da, db, idesc_pv,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&bars->o_done[t]);
+                }
+                if (!ok)
+                    break;
+                umma_commit(&bars->kv_empty[sv]);
+            }
+            // Drain: all MMAs issued by this thread complete before TMEM is freed.
+            umma_commit(&bars->drain);
+            mbar_wait_drain(&bars->drain, 0, p.status);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = warp / 4;              // query tile of this warpgroup
+        const int wq = warp % 4;             // TMEM lane quarter of this warp
+        const int r = wq * 32 + lane;        // row within the tile
+        const int i = q0[t] + r;             // query row
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
+        const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
+        const uint32_t sP_row = smem_u32(sP + t * C::kPBytes);
+        uint8_t *sOut = sQ + t * C::kTileBytes;  // Q_t's buffer, reused for the O tile
+        const uint32_t sOut_a = smem_u32(sOut);
+        const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
+        const float sl2 = p.scale_log2;
+
+        float m = -INFINITY;  // running max of the raw scores (scale > 0)
+        float l = 0.0f;       // running sum of exp2((s - m) * sl2)
+        bool ok = true;
+        if (q0[t] < p.Sq)
+            ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
+        // Waits feed .sync.aligned TMEM instructions: keep their outcome warp-uniform.
+        ok = __all_sync(0xffffffffu, ok);
+
+        for (int j = 0; j < n_kv[t] && ok; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort_flag, p.status));
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            float s[kBlockN];
+            {
+                uint32_t raw[64];
+                tmem_ld64_wait(tS, raw);
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    s[c] = __uint_as_float(raw[c]);
+                tmem_ld64_wait(tS + 64, raw);
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    s[64 + c] = __uint_as_float(raw[c]);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->s_free[t]);
+
+            if (j >= mask_from[t]) {
+                const int key0 = j * kBlockN;
+#pragma unroll
+                for (int c = 0; c < kBlockN; ++c)
+                    if (key0 + c >= lim)
+                        s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < kBlockN; ++c)
+                mx = fmaxf(mx, s[c]);
+            const float m_new = fmaxf(m, mx);
+            const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+            const float neg = -m_use * sl2;
+            const float corr = ex2_approx((m - m_use) * sl2);  // 0 while m = -inf
+            float rs = 0.0f;
+            uint32_t pk[kBlockN / 2];
+#pragma unroll
+            for (int c = 0; c < kBlockN; c += 2) {
+                const float p0 = ex2_approx(fmaf(s[c], sl2, neg));
+                const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
+                rs += p0 + p1;
+                pk[c / 2] = pack_bf16x2(p0, p1);
+            }
+            l = l * corr + rs;
+            m = m_new;
+
+            if (j > 0) {
+                // PV of the previous tile must be done: it reads P_t and writes O_t.
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bars->o_done[t], (j - 1) & 1, abort_flag, p.status));
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+            }
+            // P row -> swizzled K-major tile (keys 0-63 in box 0, 64-127 in box 1).
+#pragma unroll
+            for (int cb = 0; cb < kBlockN / 8; ++cb) {
+                const uint32_t addr =
+                    sP_row + (cb / 8) * kBoxBytes + sw128_offset(static_cast<uint32_t>(r), cb % 8);
+                st_shared_v4(addr, pk[cb * 4], pk[cb * 4 + 1], pk[cb * 4 + 2], pk[cb * 4 + 3]);
+            }
+            // Rescale the unnormalised O row when the max moved (warp-uniform).
+            if (j > 0 && __any_sync(0xffffffffu, corr != 1.0f)) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32_wait(tO + c0, o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
+                    tmem_st32(tO + c0, o);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->p_full[t]);
+        }
+
+        // ------------------------------------------------------------ epilogue
+        if (ok && q0[t] < p.Sq) {
+            if (n_kv[t] > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (n_kv[t] - 1) & 1,
+                                                       abort_flag, p.status));
+                tc_fence_after_sync();
+            }
+            if (ok) {
+                const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    if (n_kv[t] > 0) {
+                        tmem_ld32_wait(tO + c0, o);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = 0u;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2)
+                        pk[c / 2] = pack_bf16x2(__uint_as_float(o[c]) * inv_l,
+                                                __uint_as_float(o[c + 1]) * inv_l);
+                    const int box = c0 / 64;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t chunk = ((c0 % 64) / 8) + q;
+                        st_shared_v4(sOut_a + box * kBoxBytes +
+                                         sw128_offset(static_cast<uint32_t>(r), chunk),
+                                     pk[q * 4], pk[q * 4 + 1], pk[q * 4 + 2], pk[q * 4 + 3]);
+                    }
+                }
+                if (i < p.Sq) {
+                    const float lse = (l > 0.0f) ? m * p.scale + logf(l) : -INFINITY;
+                    p.lse[static_cast<size_t>(bh) * p.Sq + i] = lse;
+                }
+            }
+        }
+        tc_fence_before_sync();
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, 128);
+        if (r == 0 && ok && q0[t] < p.Sq && !*reinterpret_cast<volatile int *>(abort_flag)) {
+            for (int b = 0; b < C::kBoxes; ++b)
+                tma_store_3d(&tm_o, sOut + b * kBoxBytes, b * 64, q0[t], bh);
+            tma_store_commit();
+            tma_store_wait_all();
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == kMmaWarp)
+        tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D>
+fa_status_t launch(const Problem &pr)
+{
+    using C = Cfg<D>;
+    CUtensorMap tq, tk, tv, to;
+    const uint64_t BH = static_cast<uint64_t>(pr.B * pr.H);
+    if (!encode_tmap_bf16_3d(&tq, pr.q, D, pr.Sq, BH, kBlockM) ||
+        !encode_tmap_bf16_3d(&tk, pr.k, D, pr.Sk, BH, kBlockN) ||
+        !encode_tmap_bf16_3d(&tv, pr.v, D, pr.Sk, BH, kBlockN) ||
+        !encode_tmap_bf16_3d(&to, pr.o, D, pr.Sq, BH, kBlockM))
+        return FA_ERR_CUDA;
+    Params p;
+    p.Sq = static_cast<int>(pr.Sq);
+    p.Sk = static_cast<int>(pr.Sk);
+    p.BH = static_cast<int>(BH);
+    p.n_qblk = static_cast<int>((pr.Sq + kTiles * kBlockM - 1) / (kTiles * kBlockM));
+    p.causal = pr.causal ? 1 : 0;
+    p.scale = pr.scale;
+    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.lse = pr.lse;
+    p.status = pr.status;
+    auto kern = fa_prefill_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return FA_ERR_CUDA;
+    const uint64_t grid = static_cast<uint64_t>(p.n_qblk) * BH;
+    if (grid > 0x7FFFFFFFull)
+        return FA_ERR_UNSUPPORTED;
+    kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, pr.stream>>>(tq, tk, tv, to, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace prefill
+
+fa_status_t launch_prefill_sm103(const Problem &p)
+{
+    if (p.d == 128)
+        return prefill::launch<128>(p);
+    if (p.d == 64)
+        return prefill::launch<64>(p);
+    return FA_ERR_UNSUPPORTED;
+}
+
+}  // namespace fa

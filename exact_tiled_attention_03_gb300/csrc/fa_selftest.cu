@@ -1,0 +1,147 @@
+// fa_selftest.cu — test-only kernels (declared in include/fa_testing.h).
+//
+//  * fa_selftest_umma_kernel: one CTA computes C[128, N] = A[128, K] . B^T
+//    (or A . B) with the same TMA boxes, swizzle, shared-memory descriptors,
+//    instruction descriptors and TMEM read-back as the attention kernel, so
+//    the tests can check each encoding against a CPU matmul on its own.
+//  * fa_selftest_wait_kernel: the bounded mbarrier wait of the attention
+//    kernels on a barrier that nothing completes; it must give up after the
+//    limit, set the device status word and return.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace selftest {
+
+constexpr int kThreads = 128;
+
+struct UmmaBars {
+    uint64_t tma;
+    uint64_t mma;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// A: K-major, (K/64) boxes of [128 rows x 64 cols]. B: K-major (N rows x K)
+// in (K/64) boxes of [N x 64], or MN-major (K rows x N) in (N/64) boxes of
+// [K x 64].
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_selftest_umma_kernel(const __grid_constant__ CUtensorMap tm_a,
+                            const __grid_constant__ CUtensorMap tm_b, float *c, int N, int K,
+                            int b_mn_major, unsigned int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t *sA = smem;                 // 128 x K bf16
+    uint8_t *sB = smem + 128 * K * 2;   // N x K bf16
+    UmmaBars *bars = reinterpret_cast<UmmaBars *>(smem + 128 * K * 2 + N * K * 2);
+    const int warp = threadIdx.x / 32;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->mma, 1);
+        bars->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bars->tma, static_cast<uint32_t>((128 + N) * K * 2));
+        for (int b = 0; b < K / 64; ++b)
+            tma_load_3d(sA + b * 128 * 128, &tm_a, &bars->tma, b * 64, 0, 0);
+        if (!b_mn_major) {
+            for (int b = 0; b < K / 64; ++b)
+                tma_load_3d(sB + b * N * 128, &tm_b, &bars->tma, b * 64, 0, 0);
+        } else {
+            for (int b = 0; b < N / 64; ++b)
+                tma_load_3d(sB + b * K * 128, &tm_b, &bars->tma, b * 64, 0, 0);
+        }
+        ok = mbar_wait_drain(&bars->tma, 0, status);
+        tc_fence_after_sync();
+        if (ok) {
+            const uint32_t idesc = idesc_bf16_f32(128, N, false, b_mn_major != 0);
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+            for (int kk = 0; kk < K / 16; ++kk) {
+                const uint32_t koff = (kk / 4) * 128 * 128 + (kk % 4) * 32;
+                const uint64_t da = smem_desc_sw128(a0 + koff, 16, 1024);
+                uint64_t db;
+                if (!b_mn_major)
+                    db = smem_desc_sw128(b0 + (kk / 4) * N * 128 + (kk % 4) * 32, 16, 1024);
+                else
+                    db = smem_desc_sw128(b0 + kk * 16 * 128, K * 128, 1024);
+                umma_bf16_ss(tmem, da, db, idesc, kk > 0 ? 1u : 0u);
+            }
+        }
+        umma_commit(&bars->mma);
+    }
+    __syncwarp();
+    ok = mbar_wait_drain(&bars->mma, 0, status);
+    tc_fence_after_sync();
+    const int row = threadIdx.x;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32_wait(taddr + c0, r);
+        if (ok)
+            for (int j = 0; j < 32; ++j)
+                c[row * N + c0 + j] = __uint_as_float(r[j]);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0)
+        tmem_dealloc(tmem, 128);
+}
+
+__global__ void fa_selftest_wait_kernel(uint64_t limit_ns, unsigned int *status)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait(&bar, 0, &abort_flag, status, limit_ns);  // nothing arrives
+    __syncthreads();
+}
+
+}  // namespace selftest
+
+fa_status_t launch_selftest_umma(const void *a, const void *b, float *c, int n, int k,
+                                 int b_mn_major, cudaStream_t stream, unsigned int *status)
+{
+    CUtensorMap ta, tb;
+    if (!encode_tmap_bf16_3d(&ta, a, k, 128, 1, 128))
+        return FA_ERR_CUDA;
+    const bool ok_b = b_mn_major ? encode_tmap_bf16_3d(&tb, b, n, k, 1, k)
+                                 : encode_tmap_bf16_3d(&tb, b, k, n, 1, n);
+    if (!ok_b)
+        return FA_ERR_CUDA;
+    const int smem = 128 * k * 2 + n * k * 2 + 64 + 1024;
+    if (cudaFuncSetAttribute(selftest::fa_selftest_umma_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return FA_ERR_CUDA;
+    selftest::fa_selftest_umma_kernel<<<1, selftest::kThreads, smem, stream>>>(ta, tb, c, n, k,
+                                                                               b_mn_major, status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t stream, unsigned int *status)
+{
+    selftest::fa_selftest_wait_kernel<<<1, 32, 0, stream>>>(timeout_ns, status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace fa

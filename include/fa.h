@@ -1,0 +1,159 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * What the library computes, for every batch b, head h and query row i:
+ *
+ *     s_j   = scale * (Q[b,h,i,:] . K[b,h,j,:])            for visible keys j
+ *     O[b,h,i,:] = sum_j softmax(s)_j * V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp(s_j)
+ *
+ * i.e. O = softmax(scale * Q K^T + mask) V, computed exactly (no
+ * approximation of the softmax) without ever forming the score matrix in
+ * device memory:
+ *   - the definition: "Warmup Guide — Inference Optimization at Depth",
+ *     Chapter 1 (S = Q K^T, P = softmax(S), O = P V) and Chapter 2 (safe
+ *     softmax);
+ *   - the tiled forward with the online softmax, each query block held on
+ *     chip while K/V blocks stream through, O divided by the running sum
+ *     once and written once: same page, Chapters 3 and 4, and
+ *     "FlashAttention, speculative decoding, quantisation and parallelism",
+ *     Mechanics;
+ *   - the per-row statistics kept for the backward pass (Chapter 4), written
+ *     as LSE = m + ln(l);
+ *   - the decode-shaped path (few queries against a long KV cache, e.g. the
+ *     k+1 positions of a speculative-decoding verify step): split the keys
+ *     across CTAs and combine the partials, "Lecture 06 — Making Decode
+ *     Fast", section 5 (Flash-Decoding).
+ *
+ * Conventions shared by every entry point
+ *   Layout    Q, O: [B, H, Sq, d]; K, V: [B, H, Sk, d]; all contiguous,
+ *             row-major, bf16 (IEEE bfloat16 bit patterns). LSE: [B, H, Sq]
+ *             fp32, natural log, in units of the scaled logits.
+ *   Causal    causal != 0 hides key j from query i unless
+ *             j <= i + (Sk - Sq) (bottom-right alignment: the Sq queries sit
+ *             after the first Sk - Sq keys). A row with no visible key gets
+ *             O = 0 and LSE = -inf.
+ *   Scale     finite and > 0 (normally 1/sqrt(d)).
+ *   Sizes     B, H, Sq, Sk >= 1; d in {64, 128}; Sq, Sk < 2^31; B*H < 2^31.
+ *   Pointers  device pointers owned by the caller, 16-byte aligned (the
+ *             kernels move tiles with TMA, which needs 16-byte aligned
+ *             bases). The library never frees or retains them.
+ *   Stream    a cudaStream_t passed as void* (NULL = legacy default stream).
+ *             Every call enqueues work on it and returns without a host
+ *             synchronisation, unless stated otherwise.
+ *   Device    the current CUDA device of the calling thread; pointers must
+ *             belong to it. The kernels need sm_103 (GB300).
+ *   Errors    argument checks run first and return before anything is
+ *             enqueued. A failed launch returns FA_ERR_CUDA. A bounded
+ *             device-side wait that runs out sets a status word in device
+ *             memory; fa_device_status() reads it.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer, size <= 0, non-finite scale, bad split count */
+    FA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, misaligned pointer, scale <= 0, no sm_103 device */
+    FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
+    FA_ERR_TIMEOUT = 4,      /* a kernel's bounded wait ran out (reported by fa_device_status) */
+    FA_ERR_WORKSPACE = 5     /* workspace missing or smaller than fa_workspace_size() */
+} fa_status_t;
+
+/*
+ * Attention forward, dispatching on the shape:
+ *   Sq <= FA_VERIFY_MAX_SQ : the split-KV path (fa_verify_forward) with an
+ *                            automatic split count; its workspace is taken
+ *                            from the stream-ordered allocator
+ *                            (cudaMallocAsync / cudaFreeAsync on `stream`);
+ *   otherwise              : the tiled prefill path (fa_prefill_forward),
+ *                            which needs no workspace.
+ * q, k, v: inputs; o, lse: outputs (every element of both is written).
+ */
+fa_status_t fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                       float scale, void *stream);
+
+/* Largest Sq that fa_forward sends to the split-KV path. */
+#define FA_VERIFY_MAX_SQ 16
+
+/*
+ * Bytes of workspace fa_forward_ws needs for this shape (0 when the shape
+ * takes the prefill path). Pure host arithmetic; returns 0 for invalid sizes.
+ */
+size_t fa_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
+
+/*
+ * Same as fa_forward, but never allocates: the split-KV path uses the
+ * caller's `workspace` (device memory, 256-byte aligned, at least
+ * fa_workspace_size() bytes, not used concurrently by another call).
+ * Returns FA_ERR_WORKSPACE if it is missing or too small.
+ */
+fa_status_t fa_forward_ws(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                          float scale, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * The tiled prefill kernel for any Sq (the pages' FlashAttention forward):
+ * each CTA keeps two 128-row query tiles on chip (tensor memory for S and O),
+ * streams 128-key K/V tiles through a TMA-fed shared-memory ring, forms
+ * S = Q K^T with tcgen05 MMAs, applies the online softmax, accumulates
+ * O += P V with tcgen05 MMAs, skips key tiles above the causal diagonal, and
+ * writes O / l and LSE once. No workspace.
+ */
+fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                               int causal, float scale, void *stream);
+
+/*
+ * The decode-shaped split-KV kernel (Flash-Decoding) for 1 <= Sq <= 16:
+ * the keys of each (b, h) are cut into n_split contiguous chunks, one CTA
+ * per (chunk, b, h) computes a partial (O_s, LSE_s), and a combine kernel
+ * merges the partials with LSE weights:
+ *     LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+ * n_split = 0 picks a count that fills the GPU; otherwise 1 <= n_split <=
+ * ceil(Sk / 64) (chunks are multiples of 64 keys). With one chunk the
+ * partial is the result and no workspace is needed.
+ * Returns FA_ERR_UNSUPPORTED for Sq > 16.
+ */
+fa_status_t fa_verify_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                              int causal, float scale, int n_split, void *workspace,
+                              size_t ws_bytes, void *stream);
+
+/*
+ * Workspace bytes fa_verify_forward needs for this shape and split count
+ * (n_split = 0: the automatic count on the current device, which needs a
+ * CUDA device to query; returns 0 when none is present). Layout of the
+ * workspace: partial O_s as fp32 [n_split, B, H, Sq, d], then LSE_s as fp32
+ * [n_split, B, H, Sq], each part 256-byte aligned.
+ */
+size_t fa_verify_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                                int n_split);
+
+/* The split count fa_verify_forward uses for n_split = 0 on the current device (0 on error). */
+int fa_verify_auto_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
+
+/* Static text for a status code. */
+const char *fa_status_string(fa_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel gave up
+ * on a bounded wait since the last call (its outputs are then undefined).
+ * Returns FA_ERR_CUDA if the synchronisation itself fails.
+ */
+fa_status_t fa_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

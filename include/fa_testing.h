@@ -1,0 +1,55 @@
+/*
+ * fa_testing.h — test-only entry points of the attention library.
+ *
+ * None of these is on the product path; fa_forward never dispatches to them.
+ * They exist so that the GPU test suite can check the pieces of the tensor-core
+ * kernels in isolation and exercise the failure detection without faulting
+ * or hanging a GPU. Conventions (pointers, stream, errors) are those of fa.h.
+ */
+#ifndef FA_TESTING_H
+#define FA_TESTING_H
+
+#include "fa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Plain SIMT (CUDA-core, fp32) version of the tiled forward with the online
+ * softmax of "Warmup Guide — Inference Optimization at Depth", Chapters 3-4:
+ * one thread per query row, keys visited in order, running max / sum /
+ * unnormalised O, one division at the end. Same arguments, layouts and
+ * outputs as fa_forward; any d in [1, 128]; slow. A second, independent GPU
+ * implementation for cross-checks.
+ */
+fa_status_t fa_reference_forward_simt(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                      int64_t d, int causal, float scale, void *stream);
+
+/*
+ * One-CTA tcgen05 GEMM used to check the shared-memory/instruction
+ * descriptor encodings and the TMA -> SMEM -> tcgen05.mma -> TMEM ->
+ * tcgen05.ld path on their own:
+ *     b_mn_major == 0 : C[128, N] = A[128, K] . B[N, K]^T   (B row-major N x K)
+ *     b_mn_major == 1 : C[128, N] = A[128, K] . B[K, N]     (B row-major K x N)
+ * A, B bf16 row-major device arrays, C fp32 row-major [128, N].
+ * N in {64, 128}, K in {64, 128}.
+ */
+fa_status_t fa_selftest_umma(const void *a, const void *b, float *c, int n, int k,
+                             int b_mn_major, void *stream);
+
+/*
+ * Launches one CTA whose thread waits, with the same bounded wait the
+ * attention kernels use, on an mbarrier that nothing ever completes. After
+ * `timeout_ns` nanoseconds the wait gives up and sets the device status word
+ * to FA_ERR_TIMEOUT; fa_device_status() then reports it. Nothing faults or
+ * hangs: the kernel returns normally.
+ */
+fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_TESTING_H */

@@ -1,0 +1,204 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the fp64
+oracle on the same seeded bf16 inputs, element by element.
+
+Sizes are chosen so the oracle finishes in seconds while the kernels still run
+several query/key tiles and a ragged tail; the full-size workloads are checked
+on sampled rows in the same launch configuration the benchmark times.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_tiled_attention_03_gb300 import _capi
+from exact_tiled_attention_03_gb300.inputs import WORKLOADS, custom, make_qkv, sample_rows
+from parity import compare, gather_rows, oracle_full, oracle_rows, run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    _capi.load()
+
+
+# ---------------------------------------------------------------- building blocks
+@pytest.mark.parametrize("n", [64, 128])
+@pytest.mark.parametrize("k", [64, 128])
+@pytest.mark.parametrize("b_mn_major", [0, 1])
+def test_tcgen05_descriptors_one_tile_gemm(n, k, b_mn_major):
+    """One TMA -> SMEM -> tcgen05.mma -> TMEM tile, against a CPU matmul."""
+    g = torch.Generator().manual_seed(n * 7 + k + b_mn_major)
+    a = torch.randn(128, k, generator=g).to(torch.bfloat16)
+    b = torch.randn(n, k, generator=g).to(torch.bfloat16)          # B as N x K
+    b_dev = (b.t().contiguous() if b_mn_major else b).cuda()        # K x N when MN-major
+    c = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
+    _capi.check(_capi.fa_selftest_umma(a.cuda(), b_dev, c, n, k, b_mn_major), "selftest_umma")
+    torch.cuda.synchronize()
+    ref = a.double() @ b.double().t()
+    err = (c.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3 * math.sqrt(k), err
+
+
+def test_bounded_wait_reports_a_timeout_without_faulting():
+    """A wait on a barrier nothing completes gives up, sets the status word, returns."""
+    assert _capi.fa_device_status() == _capi.FA_OK
+    _capi.check(_capi.fa_selftest_wait_timeout(50_000_000), "selftest_wait")
+    assert _capi.fa_device_status() == _capi.FA_ERR_TIMEOUT
+    assert _capi.fa_device_status() == _capi.FA_OK  # read-and-clear
+
+
+# ---------------------------------------------------------------- tiny workload, every path
+@pytest.mark.parametrize("name", ["tiny_b1h1s256d64_noncausal", "tiny_b1h1s256d64_causal"])
+@pytest.mark.parametrize("entry", ["fa_forward", "fa_prefill_forward", "fa_reference_forward_simt"])
+def test_tiny_workload(name, entry):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w)
+    o, lse = run(entry, q, k, v, w.causal, w.scale)
+    ro, rl = oracle_full(q, k, v, w.causal, w.scale)
+    compare(o, lse, ro, rl)
+
+
+# ---------------------------------------------------------------- prefill kernel edge cases
+PREFILL_CASES = [
+    # B, H, Sq, Sk, d, causal
+    (1, 2, 17, 17, 64, True),
+    (1, 2, 127, 127, 128, True),
+    (1, 1, 128, 128, 128, True),
+    (1, 1, 129, 129, 128, True),
+    (1, 2, 255, 255, 64, True),
+    (1, 1, 256, 256, 128, True),
+    (1, 1, 257, 257, 128, True),
+    (2, 1, 1000, 1000, 128, True),
+    (1, 1, 1000, 1000, 64, False),
+    (1, 3, 129, 300, 128, False),
+    (1, 2, 300, 129, 64, False),
+    (1, 1, 200, 1000, 128, True),   # bottom-right: Sq < Sk
+    (1, 1, 300, 100, 128, True),    # Sq > Sk: the first 200 rows see nothing
+    (1, 1, 513, 700, 64, True),
+    (1, 1, 17, 1, 128, True),
+    (1, 1, 33, 1, 64, False),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=lambda c: "b{}h{}q{}k{}d{}{}".format(*c[:5], "c" if c[5] else "n"))
+def test_prefill_edge_shapes(case):
+    B, H, Sq, Sk, d, causal = case
+    w = custom(B, H, Sq, Sk, d, causal, seed=Sq * 31 + Sk)
+    q, k, v = make_qkv(w)
+    o, lse = run("fa_prefill_forward", q, k, v, causal, w.scale)
+    ro, rl = oracle_full(q, k, v, causal, w.scale)
+    compare(o, lse, ro, rl)
+
+
+def test_prefill_large_logits_rescale():
+    """Q x 8: logits of order +-60, the running max moves on most tiles."""
+    w = custom(1, 2, 640, 640, 128, True, seed=99, q_factor=8.0)
+    q, k, v = make_qkv(w)
+    o, lse = run("fa_prefill_forward", q, k, v, True, w.scale)
+    ro, rl = oracle_full(q, k, v, True, w.scale)
+    compare(o, lse, ro, rl)
+
+
+def test_prefill_matches_simt_reference():
+    w = custom(2, 2, 384, 512, 128, True, seed=5)
+    q, k, v = make_qkv(w)
+    o1, l1 = run("fa_prefill_forward", q, k, v, True, w.scale)
+    o2, l2 = run("fa_reference_forward_simt", q, k, v, True, w.scale)
+    assert (o1 - o2).abs().max().item() < 2e-2
+    assert (l1 - l2).abs().max().item() < 1e-3
+
+
+# ---------------------------------------------------------------- split-KV (verify) kernel
+VERIFY_CASES = [
+    # B, H, Sq, Sk, d, causal
+    (2, 3, 5, 1000, 128, True),
+    (1, 4, 1, 777, 64, True),
+    (2, 2, 16, 300, 128, False),
+    (1, 2, 8, 64, 128, True),
+    (1, 1, 9, 5, 128, True),       # Sk < Sq: the first rows see nothing
+    (1, 2, 3, 4096, 64, False),
+]
+
+
+@pytest.mark.parametrize("case", VERIFY_CASES, ids=lambda c: "b{}h{}q{}k{}d{}{}".format(*c[:5], "c" if c[5] else "n"))
+@pytest.mark.parametrize("n_split", [0, 1, 2, 3, 7, "max"])
+def test_verify_split_counts(case, n_split):
+    B, H, Sq, Sk, d, causal = case
+    max_split = -(-Sk // 64)
+    ns = max_split if n_split == "max" else n_split
+    if ns > max_split:
+        pytest.skip("more splits than 64-key chunks")
+    w = custom(B, H, Sq, Sk, d, causal, seed=Sk + Sq, q_factor=2.0)
+    q, k, v = make_qkv(w)
+    o, lse = run("fa_verify_forward", q, k, v, causal, w.scale, n_split=ns)
+    ro, rl = oracle_full(q, k, v, causal, w.scale)
+    compare(o, lse, ro, rl)
+
+
+def test_verify_rejects_small_workspace():
+    w = custom(1, 2, 5, 1024, 128, True)
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 5, dtype=torch.float32, device="cuda")
+    need = _capi.fa_verify_workspace_size(1, 2, 5, 1024, 128, 4)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = _capi.fa_verify_forward(q, k, v, o, lse, 1, 2, 5, 1024, 128, 1, w.scale, 4, ws, need - 1)
+    assert st == _capi.FA_ERR_WORKSPACE
+    st = _capi.fa_verify_forward(q, k, v, o, lse, 1, 2, 5, 1024, 128, 1, w.scale, 4, None, 0)
+    assert st == _capi.FA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("entry", ["fa_forward", "fa_forward_ws"])
+@pytest.mark.parametrize("Sq", [1, 5, 16, 17])
+def test_dispatch_entry_points(entry, Sq):
+    w = custom(2, 2, Sq, 700, 128, True, seed=Sq)
+    q, k, v = make_qkv(w)
+    o, lse = run(entry, q, k, v, True, w.scale)
+    ro, rl = oracle_full(q, k, v, True, w.scale)
+    compare(o, lse, ro, rl)
+
+
+# ---------------------------------------------------------------- the pages' workloads
+def test_verify_workload_full():
+    """B=16, H=32, Sq=5 after a 4091-token cache (query i sees keys [0, 4091+i]), every row."""
+    w = WORKLOADS["verify_b16h32q5k4096d128"]
+    q, k, v = make_qkv(w)
+    o, lse = run("fa_forward", q, k, v, w.causal, w.scale)
+    ro, rl = oracle_full(q, k, v, w.causal, w.scale)
+    compare(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("name", ["prefill_b4h32s2048d128_causal", "prefill_b4h32s2048d128_causal_q4"])
+def test_prefill_2k_workloads_full(name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w)
+    o, lse = run("fa_forward", q, k, v, w.causal, w.scale)
+    ro, rl = oracle_full(q, k, v, w.causal, w.scale)
+    compare(o, lse, ro, rl)
+
+
+def test_prefill_8k_headline_sampled_rows():
+    """The headline workload in its timed configuration; 64 seeded (b, h, i) rows."""
+    w = WORKLOADS["prefill_b4h32s8192d128_causal"]
+    q, k, v = make_qkv(w)
+    o, lse = run("fa_forward", q, k, v, w.causal, w.scale)
+    rows = sample_rows(w, n_total=64)
+    ro, rl = oracle_rows(q, k, v, w.causal, w.scale, rows)
+    go, gl = gather_rows(o, lse, rows)
+    compare(go, gl, ro, rl)
+    # the row every causal prefill pins: query 0 attends to key 0 only
+    assert torch.allclose(o[:, :, 0], v[:, :, 0].float(), atol=0, rtol=0)
+
+
+def test_prefill_32k_d64_sampled_rows():
+    """B=1, H=32, S=32768, d=64; 64 rows per head incl. first, last and tile boundaries."""
+    w = WORKLOADS["prefill_b1h32s32768d64_causal"]
+    q, k, v = make_qkv(w)
+    o, lse = run("fa_forward", q, k, v, w.causal, w.scale)
+    rows = sample_rows(w, per_head=64)
+    ro, rl = oracle_rows(q, k, v, w.causal, w.scale, rows)
+    go, gl = gather_rows(o, lse, rows)
+    compare(go, gl, ro, rl)
