@@ -21,6 +21,7 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
 FA_VERIFY_MAX_SQ = 16
+FA_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 # Every function the headers declare, with its ctypes signature.
 _P, _I64, _I32, _F32, _SZ, _U64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -34,6 +35,7 @@ SIGNATURES = {
     "fa_verify_forward": (_I32, _ATTN + [_I32, _P, _SZ, _P]),
     "fa_verify_workspace_size": (_SZ, [_I64] * 5 + [_I32]),
     "fa_verify_auto_splits": (_I32, [_I64] * 5),
+    "fa_verify_forward_static": (_I32, _ATTN + [_I32, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I32]),
     "fa_device_status": (_I32, [_P]),
     "fa_reference_forward_simt": (_I32, _ATTN + [_P]),
@@ -122,6 +124,13 @@ def fa_verify_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, n_split, 
     return load().fa_verify_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk,
                                     d, int(bool(causal)), float(scale), int(n_split),
                                     _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def fa_verify_forward_static(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, n_split,
+                             stream=None) -> int:
+    return load().fa_verify_forward_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                           Sq, Sk, d, int(bool(causal)), float(scale),
+                                           int(n_split), _stream(stream))
 
 
 def fa_verify_workspace_size(B, H, Sq, Sk, d, n_split) -> int:

@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfa_gb300.so")
 
-SOURCES = ["fa_abi.cu", "fa_prefill_sm103.cu", "fa_verify.cu", "fa_simt.cu", "fa_selftest.cu"]
+SOURCES = ["fa_abi.cu", "fa_prefill_sm103.cu", "fa_verify.cu", "fa_simt.cu", "fa_selftest.cu",
+           "fa_verify_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -141,6 +141,32 @@ size_t fa_verify_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, in
 /* The split count fa_verify_forward uses for n_split = 0 on the current device (0 on error). */
 int fa_verify_auto_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
 
+/*
+ * Size of the library-owned scratch used by fa_verify_forward_static.
+ */
+#define FA_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * fa_verify_forward without any allocation and without a caller workspace.
+ * The pages have no counterpart: it exists for callers that cannot call
+ * cudaMalloc (plugins in a host runtime that owns all device memory and
+ * passes them only their input and output buffers; serving loops that
+ * reserved nearly all of HBM up front; loops that cannot accept the
+ * synchronisation an allocation may cause).
+ * Arguments, layouts and results are those of fa_verify_forward (n_split = 0
+ * picks the automatic count). The split-KV partials go to a file-scope
+ * device array of FA_STATIC_SCRATCH_BYTES bytes that every GPU loading the
+ * library holds until exit. The first call on a device looks up that
+ * array's address with the device current; make it before any stream
+ * capture. All calls share the array and it keeps the last call's contents:
+ * calls that overlap on the GPU race. Returns FA_ERR_WORKSPACE when the
+ * partials (fa_verify_workspace_size) exceed FA_STATIC_SCRATCH_BYTES.
+ */
+fa_status_t fa_verify_forward_static(const void *q, const void *k, const void *v, void *o,
+                                     float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                     int64_t d, int causal, float scale, int n_split,
+                                     void *stream);
+
 /* Static text for a status code. */
 const char *fa_status_string(fa_status_t status);
 
