@@ -40,6 +40,7 @@ SIGNATURES = {
     "fa_device_status": (_I32, [_P]),
     "fa_reference_forward_simt": (_I32, _ATTN + [_P]),
     "fa_selftest_umma": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
+    "fa_selftest_umma_ts": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_wait_timeout": (_I32, [_U64, _P]),
 }
 
@@ -155,6 +156,11 @@ def fa_reference_forward_simt(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale,
 def fa_selftest_umma(a, b, c, n, k, b_mn_major, stream=None) -> int:
     return load().fa_selftest_umma(_ptr(a), _ptr(b), _ptr(c), int(n), int(k), int(b_mn_major),
                                    _stream(stream))
+
+
+def fa_selftest_umma_ts(a, b, c, n, k, b_mn_major, stream=None) -> int:
+    return load().fa_selftest_umma_ts(_ptr(a), _ptr(b), _ptr(c), int(n), int(k), int(b_mn_major),
+                                      _stream(stream))
 
 
 def fa_selftest_wait_timeout(timeout_ns, stream=None) -> int:

@@ -341,6 +341,23 @@ fa_status_t fa_selftest_umma(const void *a, const void *b, float *c, int n, int 
                                 di->status);
 }
 
+fa_status_t fa_selftest_umma_ts(const void *a, const void *b, float *c, int n, int k,
+                                int b_mn_major, void *stream)
+{
+    if (!a || !b || !c)
+        return FA_ERR_INVALID_ARG;
+    if ((n != 64 && n != 128) || (k != 64 && k != 128) || (b_mn_major != 0 && b_mn_major != 1))
+        return FA_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c))
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_umma_ts(a, b, c, n, k, b_mn_major, static_cast<cudaStream_t>(stream),
+                                   di->status);
+}
+
 fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
 {
     if (timeout_ns == 0 || timeout_ns > 10000000000ull)

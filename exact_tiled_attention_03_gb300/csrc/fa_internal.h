@@ -35,6 +35,8 @@ fa_status_t launch_verify(const Problem &p, int n_split, void *workspace, size_t
 fa_status_t launch_reference_simt(const Problem &p);
 fa_status_t launch_selftest_umma(const void *a, const void *b, float *c, int n, int k,
                                  int b_mn_major, cudaStream_t stream, unsigned int *status);
+fa_status_t launch_selftest_umma_ts(const void *a, const void *b, float *c, int n, int k,
+                                    int b_mn_major, cudaStream_t stream, unsigned int *status);
 fa_status_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t stream, unsigned int *status);
 
 // Split-KV geometry shared by the ABI (workspace sizing) and the launcher.

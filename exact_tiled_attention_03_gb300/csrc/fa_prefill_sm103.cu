@@ -46,6 +46,8 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (16 KB)
+// Lazy rescale threshold, in log2 units of the exponent (factor 256).
+constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct Cfg {
@@ -116,10 +118,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // Heaviest query blocks first: with the causal mask the last blocks of a
-    // sequence see the most keys.
-    const int bh = blockIdx.x % p.BH;
-    const int qblk = p.n_qblk - 1 - static_cast<int>(blockIdx.x / p.BH);
+    // Head-major order, heaviest query block first within each head: the CTAs
+    // running at the same time share a few heads' K/V in L2, and with the
+    // causal mask the last query blocks (most keys) start first.
+    const int bh = static_cast<int>(blockIdx.x / p.n_qblk);
+    const int qblk = p.n_qblk - 1 - static_cast<int>(blockIdx.x % p.n_qblk);
 
     int q0[kTiles], n_kv[kTiles], mask_from[kTiles];
 #pragma unroll
@@ -209,70 +212,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
+        // Ring order of the loads: K_0, V_0, K_1, V_1, ... (K_j at index 2j, V_j
+        // at 2j+1). Issue order: S_t(0) first, then per j: S_0(j+1), S_1(j+1)
+        // (next scores, overlapping this tile's softmax), then O_t += P_t V_j.
         if (lane == 0 && any_tile && n_kv_max > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
             const uint32_t colS[kTiles] = {C::kColS0, C::kColS1};
             const uint32_t colO[kTiles] = {C::kColO0, C::kColO1};
             const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV), sP_a = smem_u32(sP);
+            auto issue_s = [&](int t, int slot) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+                    const uint64_t da = smem_desc_sw128(sQ_a + t * C::kTileBytes + koff, 16, 1024);
+                    const uint64_t db = smem_desc_sw128(sKV_a + slot * C::kTileBytes + koff, 16, 1024);
+                    umma_bf16_ss(tmem + colS[t], da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int slot, int j) {
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    const uint64_t da = smem_desc_sw128(
+                        sP_a + t * C::kPBytes + (kk / 4) * kBoxBytes + (kk % 4) * 32, 16, 1024);
+                    const uint64_t db = smem_desc_sw128(sKV_a + slot * C::kTileBytes + kk * 16 * 128,
+                                                        kBoxBytes, 1024);
+                    umma_bf16_ss(tmem + colO[t], da, db, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
             bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
-            tc_fence_after_sync();
-            int it = 0;
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                // S_t = Q_t K_j^T
-                const int sk = it % C::kStages;
-                ok = mbar_wait(&bars->kv_full[sk], (it / C::kStages) & 1, abort_flag, p.status);
-                ++it;
-                if (!ok)
-                    break;
+            if (ok)
+                ok = mbar_wait(&bars->kv_full[0], 0, abort_flag, p.status);  // K_0
+            if (ok) {
                 tc_fence_after_sync();
-                for (int t = 0; t < kTiles; ++t) {
-                    if (j >= n_kv[t])
-                        continue;
-                    if (j > 0) {
-                        ok = mbar_wait(&bars->s_free[t], (j - 1) & 1, abort_flag, p.status);
+                for (int t = 0; t < kTiles; ++t)
+                    if (n_kv[t] > 0) {
+                        issue_s(t, 0);
+                        umma_commit(&bars->s_full[t]);
+                    }
+                umma_commit(&bars->kv_empty[0]);
+            }
+            for (int j = 0; j < n_kv_max && ok; ++j) {
+                if (j + 1 < n_kv_max) {
+                    const int idx = 2 * (j + 1), sk = idx % C::kStages;
+                    ok = mbar_wait(&bars->kv_full[sk], (idx / C::kStages) & 1, abort_flag, p.status);
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    for (int t = 0; t < kTiles && ok; ++t) {
+                        if (j + 1 >= n_kv[t])
+                            continue;
+                        ok = mbar_wait(&bars->s_free[t], j & 1, abort_flag, p.status);
                         if (!ok)
                             break;
                         tc_fence_after_sync();
+                        issue_s(t, sk);
+                        umma_commit(&bars->s_full[t]);
                     }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-                        const uint64_t da =
-                            smem_desc_sw128(sQ_a + t * C::kTileBytes + koff, 16, 1024);
-                        const uint64_t db =
-                            smem_desc_sw128(sKV_a + sk * C::kTileBytes + koff, 16, 1024);
-                        umma_bf16_ss(tmem + colS[t], da, db, idesc_qk, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(&bars->s_full[t]);
+                    if (!ok)
+                        break;
+                    umma_commit(&bars->kv_empty[sk]);
                 }
-                if (!ok)
-                    break;
-                umma_commit(&bars->kv_empty[sk]);
-                // O_t += P_t V_j
-                const int sv = it % C::kStages;
-                ok = mbar_wait(&bars->kv_full[sv], (it / C::kStages) & 1, abort_flag, p.status);
-                ++it;
+                const int idx = 2 * j + 1, sv = idx % C::kStages;
+                ok = mbar_wait(&bars->kv_full[sv], (idx / C::kStages) & 1, abort_flag, p.status);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
-                for (int t = 0; t < kTiles; ++t) {
+                for (int t = 0; t < kTiles && ok; ++t) {
                     if (j >= n_kv[t])
                         continue;
                     ok = mbar_wait(&bars->p_full[t], j & 1, abort_flag, p.status);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint64_t da = smem_desc_sw128(
-                            sP_a + t * C::kPBytes + (kk / 4) * kBoxBytes + (kk % 4) * 32, 16,
-                            1024);
-                        const uint64_t db = smem_desc_sw128(
-                            sKV_a + sv * C::kTileBytes + kk * 16 * 128, kBoxBytes, 1024);
-                        umma_bf16_ss(tmem + colO[t], da, db, idesc_pv,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    issue_pv(t, sv, j);
                     umma_commit(&bars->o_done[t]);
                 }
                 if (!ok)
@@ -298,8 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
         const float sl2 = p.scale_log2;
 
-        float m = -INFINITY;  // running max of the raw scores (scale > 0)
-        float l = 0.0f;       // running sum of exp2((s - m) * sl2)
+        // m: the reference max of this row's exponentials (raw score units,
+        // scale > 0). It is updated lazily: only when a tile's max exceeds it by
+        // more than 2^kRescaleLog2 in the exponent (or on the first visible key).
+        // O and l always share the same reference, so the result stays exact,
+        // and P = 2^((s - m) * sl2) stays <= 2^kRescaleLog2.
+        float m = -INFINITY;
+        float l = 0.0f;       // running sum of 2^((s - m) * sl2)
         bool ok = true;
         if (q0[t] < p.Sq)
             ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
@@ -313,15 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             float s[kBlockN];
             {
-                uint32_t raw[64];
-                tmem_ld64_wait(tS, raw);
+                uint32_t raw[kBlockN];
+                tmem_ld128_wait(tS, raw);
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
+                for (int c = 0; c < kBlockN; ++c)
                     s[c] = __uint_as_float(raw[c]);
-                tmem_ld64_wait(tS + 64, raw);
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    s[64 + c] = __uint_as_float(raw[c]);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -335,25 +349,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (key0 + c >= lim)
                         s[c] = -INFINITY;
             }
-            float mx = s[0];
+            // Row max: eight independent 3-input max chains, then a small tree.
+            float part[8];
 #pragma unroll
-            for (int c = 1; c < kBlockN; ++c)
-                mx = fmaxf(mx, s[c]);
-            const float m_new = fmaxf(m, mx);
-            const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-            const float neg = -m_use * sl2;
-            const float corr = ex2_approx((m - m_use) * sl2);  // 0 while m = -inf
-            float rs = 0.0f;
-            uint32_t pk[kBlockN / 2];
+            for (int k = 0; k < 8; ++k) {
+                float x = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
 #pragma unroll
-            for (int c = 0; c < kBlockN; c += 2) {
-                const float p0 = ex2_approx(fmaf(s[c], sl2, neg));
-                const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
-                rs += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
+                for (int e = 3; e < 15; e += 2)
+                    x = fmax3(x, s[16 * k + e], s[16 * k + e + 1]);
+                part[k] = fmaxf(x, s[16 * k + 15]);
             }
-            l = l * corr + rs;
-            m = m_new;
+            const float mx = fmax3(fmax3(part[0], part[1], part[2]),
+                                   fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7]));
+            const float m_new = fmaxf(m, mx);
+            // NaN (both -inf) compares false: nothing visible yet, keep m.
+            const bool move = (m_new - m) * sl2 > kRescaleLog2;
+            const float m_ref = move ? m_new : m;
+            const float corr = move ? ex2_approx((m - m_ref) * sl2) : 1.0f;  // 0 when m = -inf
+            const float neg = (m_ref == -INFINITY) ? 0.0f : -m_ref * sl2;
+            uint32_t pk[kBlockN / 2];
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            const float2 sl2x2 = make_float2(sl2, sl2), negx2 = make_float2(neg, neg);
+#pragma unroll
+            for (int c = 0; c < kBlockN / 2; ++c) {
+                const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, negx2);
+                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                acc[c % 4] = fadd2(acc[c % 4], e);
+                pk[c] = pack_bf16x2(e.x, e.y);
+            }
+            const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+            const float2 a = fadd2(a01, a23);
+            l = l * corr + (a.x + a.y);
+            m = m_ref;
 
             if (j > 0) {
                 // PV of the previous tile must be done: it reads P_t and writes O_t.
@@ -370,15 +398,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sP_row + (cb / 8) * kBoxBytes + sw128_offset(static_cast<uint32_t>(r), cb % 8);
                 st_shared_v4(addr, pk[cb * 4], pk[cb * 4 + 1], pk[cb * 4 + 2], pk[cb * 4 + 3]);
             }
-            // Rescale the unnormalised O row when the max moved (warp-uniform).
-            if (j > 0 && __any_sync(0xffffffffu, corr != 1.0f)) {
+            // Rescale the unnormalised O row when its reference max moved
+            // (warp-uniform: lanes whose max did not move multiply by 1).
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                const float2 cx2 = make_float2(corr, corr);
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
                     tmem_ld32_wait(tO + c0, o);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
+                    for (int c = 0; c < 16; ++c) {
+                        const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
+                                                           __uint_as_float(o[2 * c + 1])), cx2);
+                        o[2 * c] = __float_as_uint(v.x);
+                        o[2 * c + 1] = __float_as_uint(v.y);
+                    }
                     tmem_st32(tO + c0, o);
                 }
                 tmem_st_wait();

@@ -4,6 +4,8 @@
 //    (or A . B) with the same TMA boxes, swizzle, shared-memory descriptors,
 //    instruction descriptors and TMEM read-back as the attention kernel, so
 //    the tests can check each encoding against a CPU matmul on its own.
+//  * fa_selftest_umma_ts_kernel: the same GEMM with A read from tensor memory
+//    (the operand form a P tile held in TMEM would use).
 //  * fa_selftest_wait_kernel: the bounded mbarrier wait of the attention
 //    kernels on a barrier that nothing completes; it must give up after the
 //    limit, set the device status word and return.
@@ -102,6 +104,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, 128);
 }
 
+// Same GEMM with A taken from tensor memory: thread r writes row r of A into
+// TMEM columns [128, 128 + K/2), two bf16 per 32-bit column (element 2c in
+// the low half), then the MMA reads A from there (tcgen05.mma with [a_tmem]).
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_selftest_umma_ts_kernel(const __grid_constant__ CUtensorMap tm_b, const uint32_t *a_pairs,
+                               float *c, int N, int K, int b_mn_major, unsigned int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t *sB = smem;
+    UmmaBars *bars = reinterpret_cast<UmmaBars *>(smem + N * K * 2);
+    const int warp = threadIdx.x / 32;
+    const int row = threadIdx.x;
+    constexpr uint32_t kColA = 128;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    for (int c0 = 0; c0 < K / 2; c0 += 32) {
+        uint32_t r[32];
+        for (int j = 0; j < 32; ++j)
+            r[j] = a_pairs[row * (K / 2) + c0 + j];
+        tmem_st32(tmem + lane_base + kColA + c0, r);
+    }
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bars->tma, static_cast<uint32_t>(N * K * 2));
+        if (!b_mn_major) {
+            for (int b = 0; b < K / 64; ++b)
+                tma_load_3d(sB + b * N * 128, &tm_b, &bars->tma, b * 64, 0, 0);
+        } else {
+            for (int b = 0; b < N / 64; ++b)
+                tma_load_3d(sB + b * K * 128, &tm_b, &bars->tma, b * 64, 0, 0);
+        }
+        ok = mbar_wait_drain(&bars->tma, 0, status);
+        tc_fence_after_sync();
+        if (ok) {
+            const uint32_t idesc = idesc_bf16_f32(128, N, false, b_mn_major != 0);
+            const uint32_t b0 = smem_u32(sB);
+            for (int kk = 0; kk < K / 16; ++kk) {
+                uint64_t db;
+                if (!b_mn_major)
+                    db = smem_desc_sw128(b0 + (kk / 4) * N * 128 + (kk % 4) * 32, 16, 1024);
+                else
+                    db = smem_desc_sw128(b0 + kk * 16 * 128, K * 128, 1024);
+                umma_bf16_ts(tmem, tmem + kColA + kk * 8, db, idesc, kk > 0 ? 1u : 0u);
+            }
+        }
+        umma_commit(&bars->mma);
+    }
+    __syncwarp();
+    ok = mbar_wait_drain(&bars->mma, 0, status);
+    tc_fence_after_sync();
+    for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32_wait(tmem + lane_base + c0, r);
+        if (ok)
+            for (int j = 0; j < 32; ++j)
+                c[row * N + c0 + j] = __uint_as_float(r[j]);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0)
+        tmem_dealloc(tmem, 256);
+}
+
 __global__ void fa_selftest_wait_kernel(uint64_t limit_ns, unsigned int *status)
 {
     __shared__ uint64_t bar;
@@ -135,6 +222,23 @@ fa_status_t launch_selftest_umma(const void *a, const void *b, float *c, int n, 
         return FA_ERR_CUDA;
     selftest::fa_selftest_umma_kernel<<<1, selftest::kThreads, smem, stream>>>(ta, tb, c, n, k,
                                                                                b_mn_major, status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t launch_selftest_umma_ts(const void *a, const void *b, float *c, int n, int k,
+                                    int b_mn_major, cudaStream_t stream, unsigned int *status)
+{
+    CUtensorMap tb;
+    const bool ok_b = b_mn_major ? encode_tmap_bf16_3d(&tb, b, n, k, 1, k)
+                                 : encode_tmap_bf16_3d(&tb, b, k, n, 1, n);
+    if (!ok_b)
+        return FA_ERR_CUDA;
+    const int smem = n * k * 2 + 64 + 1024;
+    if (cudaFuncSetAttribute(selftest::fa_selftest_umma_ts_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return FA_ERR_CUDA;
+    selftest::fa_selftest_umma_ts_kernel<<<1, selftest::kThreads, smem, stream>>>(
+        tb, static_cast<const uint32_t *>(a), c, n, k, b_mn_major, status);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -40,6 +40,14 @@ fa_status_t fa_selftest_umma(const void *a, const void *b, float *c, int n, int 
                              int b_mn_major, void *stream);
 
 /*
+ * The same one-tile GEMM with A (128 x K) read by the MMA from tensor memory
+ * instead of shared memory: row r of A goes to TMEM lane r, two bf16 per
+ * 32-bit column (element 2c in the low half). Arguments as fa_selftest_umma.
+ */
+fa_status_t fa_selftest_umma_ts(const void *a, const void *b, float *c, int n, int k,
+                                int b_mn_major, void *stream);
+
+/*
  * Launches one CTA whose thread waits, with the same bounded wait the
  * attention kernels use, on an mbarrier that nothing ever completes. After
  * `timeout_ns` nanoseconds the wait gives up and sets the device status word

@@ -42,6 +42,23 @@ def test_tcgen05_descriptors_one_tile_gemm(n, k, b_mn_major):
     assert err < 1e-3 * math.sqrt(k), err
 
 
+@pytest.mark.parametrize("n", [64, 128])
+@pytest.mark.parametrize("k", [64, 128])
+@pytest.mark.parametrize("b_mn_major", [0, 1])
+def test_tcgen05_a_operand_from_tensor_memory(n, k, b_mn_major):
+    """A written to TMEM (two bf16 per column, even element low) and read by the MMA."""
+    g = torch.Generator().manual_seed(n * 11 + k + b_mn_major)
+    a = torch.randn(128, k, generator=g).to(torch.bfloat16)
+    b = torch.randn(n, k, generator=g).to(torch.bfloat16)
+    b_dev = (b.t().contiguous() if b_mn_major else b).cuda()
+    c = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
+    _capi.check(_capi.fa_selftest_umma_ts(a.cuda(), b_dev, c, n, k, b_mn_major), "selftest_umma_ts")
+    torch.cuda.synchronize()
+    ref = a.double() @ b.double().t()
+    err = (c.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3 * math.sqrt(k), err
+
+
 def test_bounded_wait_reports_a_timeout_without_faulting():
     """A wait on a barrier nothing completes gives up, sets the status word, returns."""
     assert _capi.fa_device_status() == _capi.FA_OK
