@@ -41,9 +41,11 @@ def lib():
                                        i64, i64, i64, dblp]
         L.oracle_online_rows.argtypes = common + [i64, i32, i64p, i64, dblp, dblp, i32]
         L.oracle_split_rows.argtypes = common + [i64p, i64, i64p, i64, dblp, dblp, i32]
+        L.oracle_combine.argtypes = [i64, i64, i64, dblp, dblp, dblp, dblp]
         L.oracle_max_threads.argtypes = []
         for f in (L.oracle_attention_rows, L.oracle_attention, L.oracle_probs_row,
-                  L.oracle_online_rows, L.oracle_split_rows, L.oracle_max_threads):
+                  L.oracle_online_rows, L.oracle_split_rows, L.oracle_max_threads,
+                  L.oracle_combine):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -162,4 +164,16 @@ def split(q, k, v, causal: bool, scale: float, bounds, rows=None, threads=0):
     return o, lse
 
 
-__all__ = ["attention", "probs_row", "online", "split", "max_threads", "lib"]
+def combine(o_parts, lse_parts):
+    """Combine per-part (o, lse) computed elsewhere: o_parts [P, n, d], lse_parts [P, n]."""
+    op = np.ascontiguousarray(np.asarray(o_parts, dtype=np.float64))
+    lp = np.ascontiguousarray(np.asarray(lse_parts, dtype=np.float64))
+    P, n, d = op.shape
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _check(lib().oracle_combine(P, n, d, _ptr(op, ctypes.c_double), _ptr(lp, ctypes.c_double),
+                                _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double)), "combine")
+    return o, lse
+
+
+__all__ = ["attention", "probs_row", "online", "split", "combine", "max_threads", "lib"]

@@ -483,3 +483,43 @@ int oracle_split_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
     }
     return failed ? -4 : 0;
 }
+
+/*
+ * The final combine of Flash-Decoding ("Lecture 06", section 5) on its own,
+ * for partials computed elsewhere (another process, another device):
+ * o_parts [n_parts, n_rows, d] (each normalised over its part of the keys),
+ * lse_parts [n_parts, n_rows]; writes o [n_rows, d] and lse [n_rows] with the
+ * same log-sum-exp weighting as oracle_split_rows. A part with lse = -inf
+ * has weight 0; rows where every part is -inf get o = 0, lse = -inf.
+ */
+int oracle_combine(int64_t n_parts, int64_t n_rows, int64_t d, const double *o_parts,
+                   const double *lse_parts, double *o, double *lse)
+{
+    if (n_parts < 1 || n_rows < 0 || d < 1 || !o_parts || !lse_parts || !o || !lse)
+        return -1;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        double M = -INFINITY;
+        for (int64_t c = 0; c < n_parts; ++c)
+            if (lse_parts[c * n_rows + r] > M)
+                M = lse_parts[c * n_rows + r];
+        double *orow = o + r * d;
+        for (int64_t t = 0; t < d; ++t)
+            orow[t] = 0.0;
+        if (M == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int64_t c = 0; c < n_parts; ++c)
+            sum += exp(lse_parts[c * n_rows + r] - M);
+        double L = M + log(sum);
+        for (int64_t c = 0; c < n_parts; ++c) {
+            double w = exp(lse_parts[c * n_rows + r] - L);
+            const double *prow = o_parts + (c * n_rows + r) * d;
+            for (int64_t t = 0; t < d; ++t)
+                orow[t] += w * prow[t];
+        }
+        lse[r] = L;
+    }
+    return 0;
+}

@@ -34,6 +34,8 @@ MUTATIONS = {
     "online_form2_sum_uncorrected": ("        l = l * c_old + lb * c_blk;", "        l = l + lb * c_blk;"),
     "split_weights_unnormalised": ("                double w = exp(part_lse[c] - L);",
                                    "                double w = exp(part_lse[c] - M);"),
+    "combine_weights_unnormalised": ("            double w = exp(lse_parts[c * n_rows + r] - L);",
+                                     "            double w = exp(lse_parts[c * n_rows + r] - M);"),
 }
 
 

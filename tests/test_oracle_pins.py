@@ -162,6 +162,26 @@ def test_split_combine_equals_unsplit(causal):
         assert np.max(np.abs(l - l_ref)) < TOL, bounds
 
 
+def test_combine_of_separately_computed_parts_equals_unsplit():
+    """Partials computed as independent attention problems over disjoint key ranges
+    (non-causal parts, and the final part with its own bottom-right causal offset)
+    combine to the unsplit causal result."""
+    Sk, Sq = 300, 5
+    w, q, k, v = case(1, 3, Sq, Sk, 16, True, seed=43, factor=3.0)
+    o_ref, l_ref = oracle.attention(q, k, v, True, w.scale)
+    cut = 180  # every query sees keys [0, 295 + i], so [0, 180) is fully visible
+    o_a, l_a = oracle.attention(q, k[:, :, :cut], v[:, :, :cut], False, w.scale)
+    o_b, l_b = oracle.attention(q, k[:, :, cut:], v[:, :, cut:], True, w.scale)
+    o, l = oracle.combine(np.stack([o_a.reshape(-1, 16), o_b.reshape(-1, 16)]),
+                          np.stack([l_a.reshape(-1), l_b.reshape(-1)]))
+    assert np.max(np.abs(o - o_ref.reshape(-1, 16))) < TOL
+    assert np.max(np.abs(l - l_ref.reshape(-1))) < TOL
+    # an empty part (lse = -inf) has no weight
+    o2, l2 = oracle.combine(np.stack([o_a.reshape(-1, 16), np.zeros((15, 16))]),
+                            np.stack([l_a.reshape(-1), np.full(15, -np.inf)]))
+    assert np.array_equal(o2, o_a.reshape(-1, 16)) and np.array_equal(l2, l_a.reshape(-1))
+
+
 def test_key_value_permutation_invariance():
     """Non-causal attention is a function of the set of (key, value) pairs."""
     w, q, k, v = case(1, 2, 9, 40, 16, False, seed=29)
