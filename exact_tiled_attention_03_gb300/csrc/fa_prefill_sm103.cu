@@ -17,17 +17,17 @@
 //     shared-memory stages with TMA (128-byte swizzle), one mbarrier pair per
 //     stage;
 //   * warp 9 (one elected thread) issues tcgen05.mma: S_t = Q_t K_j^T into
-//     tensor memory (TMEM), then O_t += P_t V_j, with V read MN-major straight
-//     from its row-major tile; completion is signalled with tcgen05.commit;
+//     tensor memory (TMEM), and O_t += P_t V_j with P_t read from TMEM and V
+//     read MN-major straight from its row-major tile; completion is signalled
+//     with tcgen05.commit. Issue order per key tile j: PV_0(j), S_0(j+1),
+//     PV_1(j), S_1(j+1), so each tile's softmax overlaps the other tile's
+//     two GEMMs (ping-pong);
 //   * warps 0-3 and 4-7 are one softmax warpgroup per query tile; thread r
 //     owns row r (TMEM lane r). It pulls its S row out of TMEM, masks,
 //     computes the row max and exp2 of the shifted, log2(e)-scaled logits,
-//     writes P (bf16) into a swizzled shared-memory tile for the next MMA,
-//     and rescales its O row in TMEM when the max moved. At the end it
-//     divides by l, writes the bf16 O row into shared memory for a TMA store
-//     and writes its LSE;
-//   * the two warpgroups run out of phase, so the tensor core works on one
-//     tile while the other tile's softmax runs.
+//     writes P (bf16) back over its S row in TMEM, and rescales its O row in
+//     TMEM when the reference max moved. At the end it divides by l, writes
+//     the bf16 O row into shared memory for a TMA store and writes its LSE.
 // Every wait is bounded; on expiry the CTA stops, drains what it has in
 // flight, frees its tensor memory and sets the device status word.
 #include <cmath>
@@ -53,14 +53,14 @@ template <int D>
 struct Cfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kTileBytes = kBlockM * D * 2;  // Q, K, V or O tile
-    static constexpr int kStages = (D == 128) ? 3 : 6;
-    static constexpr int kPBytes = kBlockM * kBlockN * 2;
+    static constexpr int kStages = (D == 128) ? 5 : 10;  // ~160 KB of K/V ring
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kTiles * kTileBytes;
-    static constexpr int kOffP = kOffKV + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffP + kTiles * kPBytes;
-    static constexpr int kBarBytes = 256;
+    static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+    static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+    // S_t in columns [128 t, 128 t + 128); P_t (bf16, two per column) is
+    // written over the first 64 columns of S_t once S_t is in registers.
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
     static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
     static_assert(kColO1 + D <= kTmemCols, "TMEM budget");
@@ -77,17 +77,16 @@ struct Params {
 
 struct Bars {
     uint64_t q_full;
-    uint64_t s_full[kTiles];
-    uint64_t s_free[kTiles];
-    uint64_t p_full[kTiles];
-    uint64_t o_done[kTiles];
+    uint64_t s_full[kTiles];   // S_t(j) in TMEM (one phase per key tile)
+    uint64_t p_full[kTiles];   // P_t(j) in TMEM, O_t rescaled (one phase per key tile)
+    uint64_t o_done[kTiles];   // last O_t += P_t V completed (one phase)
     uint64_t drain;
-    uint64_t kv_full[8];
-    uint64_t kv_empty[8];
+    uint64_t kv_full[16];
+    uint64_t kv_empty[16];
     uint32_t tmem_base;
     int abort_flag;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Number of keys visible to query row i (bottom-right causal alignment).
 __device__ __forceinline__ int visible_keys(int i, int Sq, int Sk, int causal)
@@ -112,7 +111,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sKV = smem + C::kOffKV;
-    uint8_t *sP = smem + C::kOffP;
     Bars *bars = reinterpret_cast<Bars *>(smem + C::kOffBar);
 
     const int warp = threadIdx.x / 32;
@@ -144,7 +142,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->q_full, 1);
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->s_free[t], 4);
             mbar_init(&bars->p_full[t], 4);
             mbar_init(&bars->o_done[t], 1);
         }
@@ -212,15 +209,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Ring order of the loads: K_0, V_0, K_1, V_1, ... (K_j at index 2j, V_j
-        // at 2j+1). Issue order: S_t(0) first, then per j: S_0(j+1), S_1(j+1)
-        // (next scores, overlapping this tile's softmax), then O_t += P_t V_j.
+        // Ring order of the loads: K_0, V_0, K_1, V_1, ... (K_j at index 2j,
+        // V_j at 2j+1), consumed in the same order. Issue order: S_0(0), S_1(0),
+        // then per j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites
+        // the TMEM columns that held P_t(j); the tensor pipe executes one
+        // thread's MMAs in order, so PV_t(j) has read P_t(j) by then.
         if (lane == 0 && any_tile && n_kv_max > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
             const uint32_t colS[kTiles] = {C::kColS0, C::kColS1};
             const uint32_t colO[kTiles] = {C::kColO0, C::kColO1};
-            const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV), sP_a = smem_u32(sP);
+            const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
             auto issue_s = [&](int t, int slot) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -233,16 +232,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv = [&](int t, int slot, int j) {
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t da = smem_desc_sw128(
-                        sP_a + t * C::kPBytes + (kk / 4) * kBoxBytes + (kk % 4) * 32, 16, 1024);
                     const uint64_t db = smem_desc_sw128(sKV_a + slot * C::kTileBytes + kk * 16 * 128,
                                                         kBoxBytes, 1024);
-                    umma_bf16_ss(tmem + colO[t], da, db, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + colO[t], tmem + colS[t] + kk * 8, db, idesc_pv,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
-            if (ok)
-                ok = mbar_wait(&bars->kv_full[0], 0, abort_flag, p.status);  // K_0
+            auto ring_wait = [&](int idx) {
+                return mbar_wait(&bars->kv_full[idx % C::kStages], (idx / C::kStages) & 1,
+                                 abort_flag, p.status);
+            };
+            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status) && ring_wait(0);  // K_0
             if (ok) {
                 tc_fence_after_sync();
                 for (int t = 0; t < kTiles; ++t)
@@ -253,31 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(&bars->kv_empty[0]);
             }
             for (int j = 0; j < n_kv_max && ok; ++j) {
-                if (j + 1 < n_kv_max) {
-                    const int idx = 2 * (j + 1), sk = idx % C::kStages;
-                    ok = mbar_wait(&bars->kv_full[sk], (idx / C::kStages) & 1, abort_flag, p.status);
-                    if (!ok)
-                        break;
-                    tc_fence_after_sync();
-                    for (int t = 0; t < kTiles && ok; ++t) {
-                        if (j + 1 >= n_kv[t])
-                            continue;
-                        ok = mbar_wait(&bars->s_free[t], j & 1, abort_flag, p.status);
-                        if (!ok)
-                            break;
-                        tc_fence_after_sync();
-                        issue_s(t, sk);
-                        umma_commit(&bars->s_full[t]);
-                    }
-                    if (!ok)
-                        break;
-                    umma_commit(&bars->kv_empty[sk]);
-                }
-                const int idx = 2 * j + 1, sv = idx % C::kStages;
-                ok = mbar_wait(&bars->kv_full[sv], (idx / C::kStages) & 1, abort_flag, p.status);
+                const int iv = 2 * j + 1, ik = 2 * j + 2;
+                ok = ring_wait(iv);  // V_j
                 if (!ok)
                     break;
                 tc_fence_after_sync();
+                bool k_ready = false;
                 for (int t = 0; t < kTiles && ok; ++t) {
                     if (j >= n_kv[t])
                         continue;
@@ -285,12 +266,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok)
                         break;
                     tc_fence_after_sync();
-                    issue_pv(t, sv, j);
-                    umma_commit(&bars->o_done[t]);
+                    issue_pv(t, iv % C::kStages, j);
+                    if (j + 1 < n_kv[t]) {
+                        if (!k_ready) {
+                            ok = ring_wait(ik);  // K_{j+1}
+                            if (!ok)
+                                break;
+                            tc_fence_after_sync();
+                            k_ready = true;
+                        }
+                        issue_s(t, ik % C::kStages);
+                        umma_commit(&bars->s_full[t]);
+                    } else {
+                        umma_commit(&bars->o_done[t]);  // this tile's last PV
+                    }
                 }
                 if (!ok)
                     break;
-                umma_commit(&bars->kv_empty[sv]);
+                umma_commit(&bars->kv_empty[iv % C::kStages]);
+                if (k_ready)
+                    umma_commit(&bars->kv_empty[ik % C::kStages]);
             }
             // Drain: all MMAs issued by this thread complete before TMEM is freed.
             umma_commit(&bars->drain);
@@ -305,7 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
         const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
-        const uint32_t sP_row = smem_u32(sP + t * C::kPBytes);
         uint8_t *sOut = sQ + t * C::kTileBytes;  // Q_t's buffer, reused for the O tile
         const uint32_t sOut_a = smem_u32(sOut);
         const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
@@ -337,11 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBlockN; ++c)
                     s[c] = __uint_as_float(raw[c]);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars->s_free[t]);
-
             if (j >= mask_from[t]) {
                 const int key0 = j * kBlockN;
 #pragma unroll
@@ -367,39 +356,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_ref = move ? m_new : m;
             const float corr = move ? ex2_approx((m - m_ref) * sl2) : 1.0f;  // 0 when m = -inf
             const float neg = (m_ref == -INFINITY) ? 0.0f : -m_ref * sl2;
-            uint32_t pk[kBlockN / 2];
+            // p = 2^(s*sl2 - m*sl2); P (bf16 pairs) goes over S_t's first 64
+            // columns, one 64-key half at a time to keep register pressure low.
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
             const float2 sl2x2 = make_float2(sl2, sl2), negx2 = make_float2(neg, neg);
 #pragma unroll
-            for (int c = 0; c < kBlockN / 2; ++c) {
-                const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, negx2);
-                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                acc[c % 4] = fadd2(acc[c % 4], e);
-                pk[c] = pack_bf16x2(e.x, e.y);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int k = 64 * h + 2 * c;
+                    const float2 x = ffma2(make_float2(s[k], s[k + 1]), sl2x2, negx2);
+                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    acc[c % 4] = fadd2(acc[c % 4], e);
+                    pk[c] = pack_bf16x2(e.x, e.y);
+                }
+                tmem_st32(tS + 32 * h, pk);
             }
             const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
             const float2 a = fadd2(a01, a23);
             l = l * corr + (a.x + a.y);
             m = m_ref;
 
-            if (j > 0) {
-                // PV of the previous tile must be done: it reads P_t and writes O_t.
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bars->o_done[t], (j - 1) & 1, abort_flag, p.status));
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-            }
-            // P row -> swizzled K-major tile (keys 0-63 in box 0, 64-127 in box 1).
-#pragma unroll
-            for (int cb = 0; cb < kBlockN / 8; ++cb) {
-                const uint32_t addr =
-                    sP_row + (cb / 8) * kBoxBytes + sw128_offset(static_cast<uint32_t>(r), cb % 8);
-                st_shared_v4(addr, pk[cb * 4], pk[cb * 4 + 1], pk[cb * 4 + 2], pk[cb * 4 + 3]);
-            }
             // Rescale the unnormalised O row when its reference max moved
             // (warp-uniform: lanes whose max did not move multiply by 1).
+            // PV_t(j-1) has completed: S_t(j), committed after it, is done.
             if (j > 0 && __any_sync(0xffffffffu, move)) {
                 const float2 cx2 = make_float2(corr, corr);
 #pragma unroll
@@ -415,9 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_st32(tO + c0, o);
                 }
-                tmem_st_wait();
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
@@ -427,8 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         if (ok && q0[t] < p.Sq) {
             if (n_kv[t] > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (n_kv[t] - 1) & 1,
-                                                       abort_flag, p.status));
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], 0, abort_flag, p.status));
                 tc_fence_after_sync();
             }
             if (ok) {
