@@ -54,22 +54,27 @@ def compile_flags(verbose_ptxas: bool = False):
     return flags
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None,
+          defines=(), lib_path: str | None = None, build_dir: str | None = None) -> str:
+    """Build the library; `defines` (e.g. ["FA_PREFILL_CHUNK=32"]) with a separate
+    `lib_path` and `build_dir` give a variant build next to the default one."""
     nvcc = nvcc_path()
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+    bdir = build_dir or BUILD
+    lib = lib_path or LIB
+    os.makedirs(bdir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     headers = _headers()
     objs, todo = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or verbose_ptxas or _stale(o, [s] + headers):
             todo.append((s, o))
 
     def _one(so):
         s, o = so
-        cmd = [nvcc] + compile_flags(verbose_ptxas) + ["-c", s, "-o", o]
+        cmd = [nvcc] + compile_flags(verbose_ptxas) + [f"-D{d}" for d in defines] + ["-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(s)}:\n{r.stdout}\n{r.stderr}")
@@ -82,14 +87,14 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     if verbose_ptxas:
         for s, log in logs:
             print(f"== {os.path.basename(s)}\n{log}")
-    if force or todo or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or todo or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -42,8 +42,15 @@ constexpr int kBlockM = 128;   // query rows per tile = TMEM lanes
 constexpr int kBlockN = 128;   // keys per K/V tile
 constexpr int kTiles = 2;      // query tiles per CTA
 constexpr int kThreads = 320;  // 2 softmax warpgroups + producer warp + MMA warp
+constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+
+// Columns of S each softmax thread pulls from TMEM at a time (32 or 64;
+// 64 measured faster on GB300 and needs no register spills).
+#ifndef FA_PREFILL_CHUNK
+#define FA_PREFILL_CHUNK 64
+#endif
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (16 KB)
 // Lazy rescale threshold, in log2 units of the exponent (factor 256).
@@ -78,7 +85,7 @@ struct Params {
 struct Bars {
     uint64_t q_full;
     uint64_t s_full[kTiles];   // S_t(j) in TMEM (one phase per key tile)
-    uint64_t p_full[kTiles];   // P_t(j) in TMEM, O_t rescaled (one phase per key tile)
+    uint64_t p_full[kTiles];   // P_t(j) in TMEM and O_t rescaled (one phase per key tile)
     uint64_t o_done[kTiles];   // last O_t += P_t V completed (one phase)
     uint64_t drain;
     uint64_t kv_full[16];
@@ -220,21 +227,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t colS[kTiles] = {C::kColS0, C::kColS1};
             const uint32_t colO[kTiles] = {C::kColO0, C::kColO1};
             const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
+            // Descriptors are built once; a stage, tile or k-step only moves the
+            // start address (bits 0-13, in 16-byte units) by a constant, which
+            // never carries out of the field (shared memory is below 256 KB).
+            const uint64_t dq0 = smem_desc_sw128(sQ_a, 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(sKV_a, 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(sKV_a, kBoxBytes, 1024);
+            constexpr uint64_t kTileStep = C::kTileBytes >> 4;
             auto issue_s = [&](int t, int slot) {
+                const uint64_t a0 = dq0 + kTileStep * t, b0 = dk0 + kTileStep * slot;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-                    const uint64_t da = smem_desc_sw128(sQ_a + t * C::kTileBytes + koff, 16, 1024);
-                    const uint64_t db = smem_desc_sw128(sKV_a + slot * C::kTileBytes + koff, 16, 1024);
-                    umma_bf16_ss(tmem + colS[t], da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                    const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+                    umma_bf16_ss(tmem + colS[t], a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int t, int slot, int j) {
+            // One 64-key half of O_t += P_t V_j (k-steps 4h .. 4h+3).
+            auto issue_pv_half = [&](int t, int slot, int j, int h) {
+                const uint64_t b0 = dv0 + kTileStep * slot;
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t db = smem_desc_sw128(sKV_a + slot * C::kTileBytes + kk * 16 * 128,
-                                                        kBoxBytes, 1024);
-                    umma_bf16_ts(tmem + colO[t], tmem + colS[t] + kk * 8, db, idesc_pv,
+                for (int q = 0; q < 4; ++q) {
+                    const int kk = 4 * h + q;
+                    umma_bf16_ts(tmem + colO[t], tmem + colS[t] + kk * 8,
+                                 b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
                                  (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
@@ -266,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok)
                         break;
                     tc_fence_after_sync();
-                    issue_pv(t, iv % C::kStages, j);
+                    issue_pv_half(t, iv % C::kStages, j, 0);
+                    issue_pv_half(t, iv % C::kStages, j, 1);
                     if (j + 1 < n_kv[t]) {
                         if (!k_ready) {
                             ok = ring_wait(ik);  // K_{j+1}
@@ -291,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&bars->drain);
             mbar_wait_drain(&bars->drain, 0, p.status);
         }
-    } else {
+    } else if (warp < kSoftmaxWarps) {
         // ------------------------------------------------------------ softmax warpgroups
         const int t = warp / 4;              // query tile of this warpgroup
         const int wq = warp % 4;             // TMEM lane quarter of this warp
@@ -318,91 +334,124 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Waits feed .sync.aligned TMEM instructions: keep their outcome warp-uniform.
         ok = __all_sync(0xffffffffu, ok);
 
+        constexpr int kChunk = FA_PREFILL_CHUNK;
+        static_assert(kChunk == 32 || kChunk == 64, "chunk of S columns");
+        const float2 sl2x2 = make_float2(sl2, sl2);
         for (int j = 0; j < n_kv[t] && ok; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort_flag, p.status));
             if (!ok)
                 break;
             tc_fence_after_sync();
-            float s[kBlockN];
-            {
-                uint32_t raw[kBlockN];
-                tmem_ld128_wait(tS, raw);
+            const bool masked_tile = j >= mask_from[t];
+            const int key0 = j * kBlockN;
+            uint32_t pk[kBlockN / 2];
+            float2 acc[4];
+            // One pass over S_t in chunks of kChunk columns: load, mask, and (when
+            // `with_exp`) p = 2^(s*sl2 + neg), accumulated into acc and packed
+            // into pk. Returns the max of the raw scores it saw.
+            auto pass = [&](bool with_exp, float neg) {
+                const float2 negx2 = make_float2(neg, neg);
+                float mx = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    s[c] = __uint_as_float(raw[c]);
-            }
-            if (j >= mask_from[t]) {
-                const int key0 = j * kBlockN;
+                for (int q = 0; q < 4; ++q)
+                    acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    if (key0 + c >= lim)
-                        s[c] = -INFINITY;
-            }
-            // Row max: eight independent 3-input max chains, then a small tree.
-            float part[8];
+                for (int c0 = 0; c0 < kBlockN; c0 += kChunk) {
+                    float sv[kChunk];
+                    {
+                        uint32_t raw[kChunk];
+                        tmem_ld_wait(tS + c0, raw);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float x = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
+                        for (int c = 0; c < kChunk; ++c)
+                            sv[c] = __uint_as_float(raw[c]);
+                    }
+                    if (masked_tile) {
 #pragma unroll
-                for (int e = 3; e < 15; e += 2)
-                    x = fmax3(x, s[16 * k + e], s[16 * k + e + 1]);
-                part[k] = fmaxf(x, s[16 * k + 15]);
-            }
-            const float mx = fmax3(fmax3(part[0], part[1], part[2]),
-                                   fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7]));
-            const float m_new = fmaxf(m, mx);
+                        for (int c = 0; c < kChunk; ++c)
+                            if (key0 + c0 + c >= lim)
+                                sv[c] = -INFINITY;
+                    }
+                    float part[kChunk / 16];
+#pragma unroll
+                    for (int k = 0; k < kChunk / 16; ++k) {
+                        float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
+#pragma unroll
+                        for (int e = 3; e < 15; e += 2)
+                            x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
+                        part[k] = fmaxf(x, sv[16 * k + 15]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kChunk / 16; ++k)
+                        mx = fmaxf(mx, part[k]);
+                    if (with_exp) {
+#pragma unroll
+                        for (int c = 0; c < kChunk / 2; ++c) {
+                            const float2 x = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2);
+                            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            acc[c % 4] = fadd2(acc[c % 4], e);
+                            pk[c0 / 2 + c] = pack_bf16x2(e.x, e.y);
+                        }
+                    }
+                }
+                return mx;
+            };
+            // Speculative pass: when every lane already has a reference max, the
+            // exponentials are computed against it while the tile's max is found.
+            const bool spec = __all_sync(0xffffffffu, m != -INFINITY);
+            const float mx = pass(spec, spec ? -m * sl2 : 0.0f);
+            // The reference moves only when the tile's max exceeds it by more
+            // than 2^kRescaleLog2 (or on the first visible key); O and l always
+            // share it, so the result stays exact and P stays <= 2^kRescaleLog2.
             // NaN (both -inf) compares false: nothing visible yet, keep m.
+            const float m_new = fmaxf(m, mx);
             const bool move = (m_new - m) * sl2 > kRescaleLog2;
-            const float m_ref = move ? m_new : m;
-            const float corr = move ? ex2_approx((m - m_ref) * sl2) : 1.0f;  // 0 when m = -inf
-            const float neg = (m_ref == -INFINITY) ? 0.0f : -m_ref * sl2;
-            // p = 2^(s*sl2 - m*sl2); P (bf16 pairs) goes over S_t's first 64
-            // columns, one 64-key half at a time to keep register pressure low.
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
-            const float2 sl2x2 = make_float2(sl2, sl2), negx2 = make_float2(neg, neg);
+            const float m_use = move ? m_new : m;
+            const float corr = move ? ex2_approx((m - m_use) * sl2) : 1.0f;  // 0 when m = -inf
+            if (!spec || __any_sync(0xffffffffu, move)) {
+                // Second pass with the moved reference (lanes that did not move
+                // recompute the same values). S_t is still intact: P has not
+                // been written yet.
+                pass(true, (m_use == -INFINITY) ? 0.0f : -m_use * sl2);
+                // O_t *= corr (warp-uniform; lanes that did not move multiply by
+                // 1). PV_t(j-1) has completed: S_t(j), committed after it, is done.
+                if (j > 0 && __any_sync(0xffffffffu, move)) {
+                    const float2 cx2 = make_float2(corr, corr);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32_wait(tO + c0, o);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
+                                                               __uint_as_float(o[2 * c + 1])),
+                                                   cx2);
+                            o[2 * c] = __float_as_uint(v.x);
+                            o[2 * c + 1] = __float_as_uint(v.y);
+                        }
+                        tmem_st32(tO + c0, o);
+                    }
+                }
+            }
+            // P (bf16 pairs) over S_t's first 64 columns, then publish.
+            {
+                uint32_t lo[32], hi[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const int k = 64 * h + 2 * c;
-                    const float2 x = ffma2(make_float2(s[k], s[k + 1]), sl2x2, negx2);
-                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    acc[c % 4] = fadd2(acc[c % 4], e);
-                    pk[c] = pack_bf16x2(e.x, e.y);
+                    lo[c] = pk[c];
+                    hi[c] = pk[32 + c];
                 }
-                tmem_st32(tS + 32 * h, pk);
-            }
-            const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
-            const float2 a = fadd2(a01, a23);
-            l = l * corr + (a.x + a.y);
-            m = m_ref;
-
-            // Rescale the unnormalised O row when its reference max moved
-            // (warp-uniform: lanes whose max did not move multiply by 1).
-            // PV_t(j-1) has completed: S_t(j), committed after it, is done.
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
-                const float2 cx2 = make_float2(corr, corr);
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32_wait(tO + c0, o);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
-                                                           __uint_as_float(o[2 * c + 1])), cx2);
-                        o[2 * c] = __float_as_uint(v.x);
-                        o[2 * c + 1] = __float_as_uint(v.y);
-                    }
-                    tmem_st32(tO + c0, o);
-                }
+                tmem_st32(tS, lo);
+                tmem_st32(tS + 32, hi);
             }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars->p_full[t]);
+            const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+            const float2 a = fadd2(a01, a23);
+            l = l * corr + (a.x + a.y);
+            m = m_use;
         }
 
         // ------------------------------------------------------------ epilogue
@@ -486,6 +535,7 @@ fa_status_t launch(const Problem &pr)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return FA_ERR_CUDA;
+
     const uint64_t grid = static_cast<uint64_t>(p.n_qblk) * BH;
     if (grid > 0x7FFFFFFFull)
         return FA_ERR_UNSUPPORTED;

@@ -69,31 +69,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
+// Checks of the abort flag, the status word and the clock happen once every
+// this many failed polls, so a wait that is about to succeed does not sit
+// behind a global-memory load.
+constexpr uint32_t kPollsPerCheck = 128;
+
 // Wait for the phase of `bar` with parity `parity` to complete. Gives up when
 // the CTA-wide abort flag is raised by another thread, when the device status
 // word already records a timeout (another CTA gave up, so the whole launch is
-// void), or after `limit_ns`, in which case it raises the flag and records a
-// timeout in the status word. Returns false when it gave up: the caller stops
-// issuing work.
+// void), or after about `limit_ns`, in which case it raises the flag and
+// records a timeout in the status word. Returns false when it gave up: the
+// caller stops issuing work.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *abort_flag,
                                           unsigned int *status, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if (*reinterpret_cast<volatile int *>(abort_flag))
-            return false;
-        if (*reinterpret_cast<volatile unsigned int *>(status) & kStatusTimeout) {
-            *reinterpret_cast<volatile int *>(abort_flag) = 1;
-            return false;
-        }
-        if (globaltimer_ns() - t0 > limit_ns) {
-            *reinterpret_cast<volatile int *>(abort_flag) = 1;
-            atomicOr(status, kStatusTimeout);
-            return false;
+        if (n % kPollsPerCheck == 0) {
+            if (*reinterpret_cast<volatile int *>(abort_flag))
+                return false;
+            if (*reinterpret_cast<volatile unsigned int *>(status) & kStatusTimeout) {
+                *reinterpret_cast<volatile int *>(abort_flag) = 1;
+                return false;
+            }
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                *reinterpret_cast<volatile int *>(abort_flag) = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
         }
     }
 }
@@ -106,13 +116,18 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if (globaltimer_ns() - t0 > limit_ns) {
-            atomicOr(status, kStatusTimeout);
-            return false;
+        if (n % kPollsPerCheck == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
         }
     }
 }
@@ -341,6 +356,10 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]
         : "r"(taddr), "r"(taddr + 32u)
         : "memory");
 }
+
+// Width-overloaded forms of the loads above.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32_wait(taddr, r); }
+__device__ __forceinline__ void tmem_ld_wait(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld64_wait(taddr, r); }
 
 // Store 32 consecutive 32-bit TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
