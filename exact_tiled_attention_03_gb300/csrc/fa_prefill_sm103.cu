@@ -23,11 +23,14 @@
 //     PV_1(j), S_1(j+1), so each tile's softmax overlaps the other tile's
 //     two GEMMs (ping-pong);
 //   * warps 0-3 and 4-7 are one softmax warpgroup per query tile; thread r
-//     owns row r (TMEM lane r). It pulls its S row out of TMEM, masks,
-//     computes the row max and exp2 of the shifted, log2(e)-scaled logits,
-//     writes P (bf16) back over its S row in TMEM, and rescales its O row in
-//     TMEM when the reference max moved. At the end it divides by l, writes
-//     the bf16 O row into shared memory for a TMA store and writes its LSE.
+//     owns row r (TMEM lane r). It streams its S row out of TMEM in 64-column
+//     chunks, masks, and computes exp2 of the log2(e)-scaled logits against
+//     its current reference max while it finds the tile's max; only if that
+//     max exceeds the reference by more than 2^8 (or on the row's first
+//     tile) does it recompute the row against the new max and rescale its O
+//     row in TMEM. It then writes P (bf16) over its S row in TMEM. At the end
+//     it divides by l, writes the bf16 O row into shared memory for a TMA
+//     store and writes its LSE.
 // Every wait is bounded; on expiry the CTA stops, drains what it has in
 // flight, frees its tensor memory and sets the device status word.
 #include <cmath>
@@ -46,11 +49,10 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 
-// Columns of S each softmax thread pulls from TMEM at a time (32 or 64;
-// 64 measured faster on GB300 and needs no register spills).
-#ifndef FA_PREFILL_CHUNK
-#define FA_PREFILL_CHUNK 64
-#endif
+// Columns of S a softmax thread pulls from TMEM at a time (64 measured faster
+// on GB300 than 32, with or without double-buffered loads, and needs no
+// register spills at 320 threads).
+constexpr int kChunk = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (16 KB)
 // Lazy rescale threshold, in log2 units of the exponent (factor 256).
@@ -334,8 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Waits feed .sync.aligned TMEM instructions: keep their outcome warp-uniform.
         ok = __all_sync(0xffffffffu, ok);
 
-        constexpr int kChunk = FA_PREFILL_CHUNK;
-        static_assert(kChunk == 32 || kChunk == 64, "chunk of S columns");
         const float2 sl2x2 = make_float2(sl2, sl2);
         for (int j = 0; j < n_kv[t] && ok; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort_flag, p.status));
@@ -355,16 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     acc[q] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c0 = 0; c0 < kBlockN; c0 += kChunk) {
+                // Process one chunk of kChunk scores starting at column c0.
+                auto consume = [&](const uint32_t *raw, int c0) {
                     float sv[kChunk];
-                    {
-                        uint32_t raw[kChunk];
-                        tmem_ld_wait(tS + c0, raw);
 #pragma unroll
-                        for (int c = 0; c < kChunk; ++c)
-                            sv[c] = __uint_as_float(raw[c]);
-                    }
+                    for (int c = 0; c < kChunk; ++c)
+                        sv[c] = __uint_as_float(raw[c]);
                     if (masked_tile) {
 #pragma unroll
                         for (int c = 0; c < kChunk; ++c)
@@ -392,6 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[c0 / 2 + c] = pack_bf16x2(e.x, e.y);
                         }
                     }
+                };
+#pragma unroll
+                for (int c0 = 0; c0 < kBlockN; c0 += kChunk) {
+                    uint32_t raw[kChunk];
+                    tmem_ld64_wait(tS + c0, raw);
+                    consume(raw, c0);
                 }
                 return mx;
             };
@@ -499,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < C::kBoxes; ++b)
                 tma_store_3d(&tm_o, sOut + b * kBoxBytes, b * 64, q0[t], bh);
             tma_store_commit();
-            tma_store_wait_all();
+            tma_store_wait_read_all();  // the staging buffer may go; the writes finish on their own
         }
     }
 

@@ -357,10 +357,6 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]
         : "memory");
 }
 
-// Width-overloaded forms of the loads above.
-__device__ __forceinline__ void tmem_ld_wait(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32_wait(taddr, r); }
-__device__ __forceinline__ void tmem_ld_wait(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld64_wait(taddr, r); }
-
 // Store 32 consecutive 32-bit TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
