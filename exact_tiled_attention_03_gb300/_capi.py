@@ -22,6 +22,7 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
 FA_VERIFY_MAX_SQ = 16
 FA_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
+FA_HOST_CHUNKS = 4
 
 # Every function the headers declare, with its ctypes signature.
 _P, _I64, _I32, _F32, _SZ, _U64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -36,6 +37,8 @@ SIGNATURES = {
     "fa_verify_workspace_size": (_SZ, [_I64] * 5 + [_I32]),
     "fa_verify_auto_splits": (_I32, [_I64] * 5),
     "fa_verify_forward_static": (_I32, _ATTN + [_I32, _P]),
+    "fa_forward_host": (_I32, _ATTN + [_P, _SZ, _P]),
+    "fa_forward_host_workspace_size": (_SZ, [_I64] * 5),
     "fa_status_string": (ctypes.c_char_p, [_I32]),
     "fa_device_status": (_I32, [_P]),
     "fa_reference_forward_simt": (_I32, _ATTN + [_P]),
@@ -132,6 +135,17 @@ def fa_verify_forward_static(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, n_
     return load().fa_verify_forward_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
                                            Sq, Sk, d, int(bool(causal)), float(scale),
                                            int(n_split), _stream(stream))
+
+
+def fa_forward_host(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, workspace=None, ws_bytes=0,
+                    stream=None) -> int:
+    return load().fa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, d,
+                                  int(bool(causal)), float(scale), _ptr(workspace), int(ws_bytes),
+                                  _stream(stream))
+
+
+def fa_forward_host_workspace_size(B, H, Sq, Sk, d) -> int:
+    return load().fa_forward_host_workspace_size(B, H, Sq, Sk, d)
 
 
 def fa_verify_workspace_size(B, H, Sq, Sk, d, n_split) -> int:

@@ -137,6 +137,72 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// Copy and compute streams (and events) fa_forward_host uses on a device,
+// created on first use with the device current.
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[FA_HOST_CHUNKS] = {}, out[FA_HOST_CHUNKS] = {};
+    std::mutex mu;  // one call enqueues at a time on these streams and events
+};
+HostPipe g_pipe[kMaxDevices];
+
+HostPipe *host_pipe()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    HostPipe &hp = g_pipe[dev];
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!hp.ready) {
+        const unsigned fl = cudaStreamNonBlocking;
+        if (cudaStreamCreateWithFlags(&hp.h2d, fl) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.comp, fl) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.d2h, fl) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+        for (int c = 0; c < FA_HOST_CHUNKS; ++c)
+            if (cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.out[c], cudaEventDisableTiming) != cudaSuccess)
+                return nullptr;
+        hp.ready = true;
+    }
+    return &hp;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte offsets of the staging buffers in fa_forward_host's workspace.
+struct HostLayout {
+    size_t q, k, v, o, lse, partials, total;
+    int n_chunks, ns;  // groups, split count for a group (verify path)
+};
+
+HostLayout host_layout(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int num_sms)
+{
+    HostLayout L;
+    const int64_t BH = B * H;
+    L.n_chunks = static_cast<int>(BH < FA_HOST_CHUNKS ? BH : FA_HOST_CHUNKS);
+    const size_t qb = static_cast<size_t>(BH) * Sq * d * 2, kb = static_cast<size_t>(BH) * Sk * d * 2;
+    L.q = 0;
+    L.k = align256(L.q + qb);
+    L.v = align256(L.k + kb);
+    L.o = align256(L.v + kb);
+    L.lse = align256(L.o + qb);
+    L.partials = align256(L.lse + static_cast<size_t>(BH) * Sq * 4);
+    L.ns = 0;
+    size_t part = 0;
+    if (Sq <= FA_VERIFY_MAX_SQ) {
+        const int64_t group = (BH + L.n_chunks - 1) / L.n_chunks;
+        L.ns = verify_auto_splits(group, Sk, num_sms);
+        part = verify_workspace_bytes(group, Sq, d, L.ns);
+    }
+    L.total = L.partials + part;
+    return L;
+}
+
 int verify_splits_or_auto(int n_split, int64_t BH, int64_t Sk, const DeviceInfo *di)
 {
     return n_split > 0 ? n_split : verify_auto_splits(BH, Sk, di->num_sms);
@@ -285,6 +351,110 @@ fa_status_t fa_forward(const void *q, const void *k, const void *v, void *o, flo
                                     di->status),
                        ns, ws, need);
     if (ws && cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK)
+        st = FA_ERR_CUDA;
+    return st;
+}
+
+size_t fa_forward_host_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d)
+{
+    if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || d <= 0)
+        return 0;
+    const DeviceInfo *di = device_info();
+    if (!di)
+        return 0;
+    return host_layout(B, H, Sq, Sk, d, di->num_sms).total;
+}
+
+fa_status_t fa_forward_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                            float scale, void *workspace, size_t ws_bytes, void *stream)
+{
+    // Host pointers need no alignment for the copies; validate everything else
+    // as for device pointers.
+    if (!q || !k || !v || !o || !lse)
+        return FA_ERR_INVALID_ARG;
+    const void *aligned = reinterpret_cast<const void *>(uintptr_t(256));
+    fa_status_t st = validate(aligned, aligned, aligned, aligned,
+                              reinterpret_cast<const float *>(aligned), B, H, Sq, Sk, d, scale,
+                              false);
+    if (st != FA_OK)
+        return st;
+    if (Sq <= FA_VERIFY_MAX_SQ && B * H > 65535)
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    const HostLayout L = host_layout(B, H, Sq, Sk, d, di->num_sms);
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    bool owned = false;
+    if (workspace) {
+        if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return FA_ERR_WORKSPACE;
+    } else {
+        if (cudaMallocAsync(&workspace, L.total, user) != cudaSuccess)
+            return FA_ERR_CUDA;
+        owned = true;
+    }
+    HostPipe *hp = host_pipe();
+    if (!hp)
+        return FA_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t BH = B * H;
+    const size_t q_row = static_cast<size_t>(Sq) * d * 2, k_row = static_cast<size_t>(Sk) * d * 2;
+    const size_t l_row = static_cast<size_t>(Sq) * 4;
+    const uint8_t *qh = static_cast<const uint8_t *>(q), *kh = static_cast<const uint8_t *>(k),
+                  *vh = static_cast<const uint8_t *>(v);
+    uint8_t *oh = static_cast<uint8_t *>(o), *lh = reinterpret_cast<uint8_t *>(lse);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    {
+        std::lock_guard<std::mutex> lock(hp->mu);
+        bool good = ok(cudaEventRecord(hp->start, user)) &&
+                    ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) &&
+                    ok(cudaStreamWaitEvent(hp->comp, hp->start, 0)) &&
+                    ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0));
+        for (int c = 0; c < L.n_chunks && good; ++c) {
+            const int64_t h0 = BH * c / L.n_chunks, h1 = BH * (c + 1) / L.n_chunks;
+            const size_t nh = static_cast<size_t>(h1 - h0);
+            // group c: host -> device
+            good = ok(cudaMemcpyAsync(ws + L.q + h0 * q_row, qh + h0 * q_row, nh * q_row,
+                                      cudaMemcpyHostToDevice, hp->h2d)) &&
+                   ok(cudaMemcpyAsync(ws + L.k + h0 * k_row, kh + h0 * k_row, nh * k_row,
+                                      cudaMemcpyHostToDevice, hp->h2d)) &&
+                   ok(cudaMemcpyAsync(ws + L.v + h0 * k_row, vh + h0 * k_row, nh * k_row,
+                                      cudaMemcpyHostToDevice, hp->h2d)) &&
+                   ok(cudaEventRecord(hp->in[c], hp->h2d)) &&
+                   ok(cudaStreamWaitEvent(hp->comp, hp->in[c], 0));
+            if (!good)
+                break;
+            // group c: the kernels, as a problem of nh heads
+            const Problem pr = make_problem(ws + L.q + h0 * q_row, ws + L.k + h0 * k_row,
+                                            ws + L.v + h0 * k_row, ws + L.o + h0 * q_row,
+                                            reinterpret_cast<float *>(ws + L.lse + h0 * l_row), 1,
+                                            static_cast<int64_t>(nh), Sq, Sk, d, causal, scale,
+                                            hp->comp, di->status);
+            if (Sq <= FA_VERIFY_MAX_SQ) {
+                const int ns = verify_auto_splits(static_cast<int64_t>(nh), Sk, di->num_sms);
+                st = launch_verify(pr, ns, ws + L.partials, L.total - L.partials);
+            } else {
+                st = launch_prefill_sm103(pr);
+            }
+            if (st != FA_OK)
+                break;
+            // group c: device -> host
+            good = ok(cudaEventRecord(hp->out[c], hp->comp)) &&
+                   ok(cudaStreamWaitEvent(hp->d2h, hp->out[c], 0)) &&
+                   ok(cudaMemcpyAsync(oh + h0 * q_row, ws + L.o + h0 * q_row, nh * q_row,
+                                      cudaMemcpyDeviceToHost, hp->d2h)) &&
+                   ok(cudaMemcpyAsync(lh + h0 * l_row, ws + L.lse + h0 * l_row, nh * l_row,
+                                      cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        // the caller's stream resumes only after everything above
+        good = good && st == FA_OK && ok(cudaEventRecord(hp->done, hp->d2h)) &&
+               ok(cudaStreamWaitEvent(user, hp->done, 0));
+        if (!good && st == FA_OK)
+            st = FA_ERR_CUDA;
+    }
+    if (owned && cudaFreeAsync(workspace, user) != cudaSuccess && st == FA_OK)
         st = FA_ERR_CUDA;
     return st;
 }

@@ -86,7 +86,8 @@ fa_status_t fa_forward(const void *q, const void *k, const void *v, void *o, flo
 
 /*
  * Bytes of workspace fa_forward_ws needs for this shape (0 when the shape
- * takes the prefill path). Pure host arithmetic; returns 0 for invalid sizes.
+ * takes the prefill path). The split-KV size depends on the current device's
+ * SM count; returns 0 for invalid sizes or when no device can be queried.
  */
 size_t fa_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
 
@@ -140,6 +141,41 @@ size_t fa_verify_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, in
 
 /* The split count fa_verify_forward uses for n_split = 0 on the current device (0 on error). */
 int fa_verify_auto_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
+
+/*
+ * Attention forward on HOST-resident tensors, with the transfers inside the
+ * call: the end-to-end form of fa_forward for a caller whose Q, K, V live in
+ * host memory and who wants O and LSE back in host memory.
+ *   q, k, v, o, lse : host pointers, same layouts as fa_forward. Page-locked
+ *                     memory (cudaHostAlloc / cudaHostRegister) lets the
+ *                     copies run asynchronously and overlap; pageable memory
+ *                     works but serialises them.
+ *   workspace       : device memory of at least fa_forward_host_workspace_size
+ *                     bytes, 256-byte aligned, used to stage Q, K, V, O, LSE
+ *                     (and split-KV partials); NULL makes the call take it from
+ *                     the stream-ordered allocator on `stream`.
+ * The (b, h) pairs are processed in FA_HOST_CHUNKS consecutive groups: the
+ * host-to-device copies of group c+1 overlap the kernels of group c and the
+ * device-to-host copies of group c-1, on copy and compute streams owned by
+ * the library. All of it is ordered after work already queued on `stream`,
+ * and `stream` waits for all of it, so synchronising `stream` (or an event
+ * recorded on it afterwards) means o and lse are filled. Calls from several
+ * host threads are serialised on the library's streams.
+ * Errors as fa_forward; a NULL host pointer is FA_ERR_INVALID_ARG.
+ */
+fa_status_t fa_forward_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                            float scale, void *workspace, size_t ws_bytes, void *stream);
+
+/* Number of (b, h) groups fa_forward_host pipelines (fewer if B*H is smaller). */
+#define FA_HOST_CHUNKS 4
+
+/*
+ * Device workspace bytes fa_forward_host needs for this shape (device copies of
+ * Q, K, V, O, LSE plus, for Sq <= FA_VERIFY_MAX_SQ, the split-KV partials of
+ * one group on the current device). 0 for invalid sizes or without a device.
+ */
+size_t fa_forward_host_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
 
 /*
  * Size of the library-owned scratch used by fa_verify_forward_static.

@@ -108,6 +108,15 @@ def test_workspace_size_is_zero_for_the_prefill_path(capi):
     assert n == o_bytes + l_bytes
 
 
+def test_host_entry_point_validates_first(capi):
+    f = capi.fa_forward_host
+    assert f(None, 1, 1, 1, 1, 1, 1, 256, 256, 128, 1, 0.1, None, 0, 0) == capi.FA_ERR_INVALID_ARG
+    assert f(1, 1, 1, 1, 1, 0, 1, 256, 256, 128, 1, 0.1, None, 0, 0) == capi.FA_ERR_INVALID_ARG
+    assert f(1, 1, 1, 1, 1, 1, 1, 256, 256, 96, 1, 0.1, None, 0, 0) == capi.FA_ERR_UNSUPPORTED
+    assert f(1, 1, 1, 1, 1, 1, 1, 256, 256, 128, 1, -1.0, None, 0, 0) == capi.FA_ERR_UNSUPPORTED
+    assert capi.fa_forward_host_workspace_size(0, 1, 1, 1, 64) == 0
+
+
 def test_testing_entry_points_validate_first(capi):
     assert capi.fa_selftest_umma(None, ALIGNED, ALIGNED, 128, 128, 0, 0) == capi.FA_ERR_INVALID_ARG
     assert capi.fa_selftest_umma(ALIGNED, ALIGNED, ALIGNED, 96, 128, 0, 0) == capi.FA_ERR_INVALID_ARG

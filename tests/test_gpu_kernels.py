@@ -178,6 +178,44 @@ def test_dispatch_entry_points(entry, Sq):
     compare(o, lse, ro, rl)
 
 
+# ---------------------------------------------------------------- host-resident tensors
+@pytest.mark.parametrize("case", [(2, 3, 300, 300, 128, True), (1, 5, 5, 1000, 128, True),
+                                  (2, 2, 129, 700, 64, False), (1, 1, 3, 64, 64, True)],
+                         ids=lambda c: "b{}h{}q{}k{}d{}{}".format(*c[:5], "c" if c[5] else "n"))
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("own_workspace", [True, False])
+def test_forward_host_buffers(case, pinned, own_workspace):
+    """fa_forward_host: host inputs and outputs, transfers pipelined inside the call."""
+    B, H, Sq, Sk, d, causal = case
+    w = custom(B, H, Sq, Sk, d, causal, seed=Sq + 7 * Sk)
+    q, k, v = make_qkv(w)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o = torch.full((B, H, Sq, d), float("nan"), dtype=torch.bfloat16, pin_memory=pinned)
+    lse = torch.full((B, H, Sq), float("nan"), dtype=torch.float32, pin_memory=pinned)
+    ws, ws_bytes = None, 0
+    if own_workspace:
+        ws_bytes = _capi.fa_forward_host_workspace_size(B, H, Sq, Sk, d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    _capi.check(_capi.fa_forward_host(q, k, v, o, lse, B, H, Sq, Sk, d, causal, w.scale, ws,
+                                      ws_bytes), "fa_forward_host")
+    torch.cuda.current_stream().synchronize()
+    _capi.check(_capi.fa_device_status(), "device status")
+    ro, rl = oracle_full(q, k, v, causal, w.scale)
+    compare(o.float(), lse, ro, rl)
+
+
+def test_forward_host_rejects_a_small_workspace():
+    w = custom(1, 2, 300, 300, 128, True)
+    q, k, v = make_qkv(w)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 300)
+    need = _capi.fa_forward_host_workspace_size(1, 2, 300, 300, 128)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert _capi.fa_forward_host(q, k, v, o, lse, 1, 2, 300, 300, 128, 1, w.scale, ws,
+                                 need - 1) == _capi.FA_ERR_WORKSPACE
+
+
 # ---------------------------------------------------------------- the pages' workloads
 def test_verify_workload_full():
     """B=16, H=32, Sq=5 after a 4091-token cache (query i sees keys [0, 4091+i]), every row."""
