@@ -22,7 +22,7 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
 FA_VERIFY_MAX_SQ = 16
 FA_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
-FA_HOST_CHUNKS = 4
+FA_HOST_CHUNKS = 16
 
 # Every function the headers declare, with its ctypes signature.
 _P, _I64, _I32, _F32, _SZ, _U64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,

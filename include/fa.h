@@ -168,7 +168,7 @@ fa_status_t fa_forward_host(const void *q, const void *k, const void *v, void *o
                             float scale, void *workspace, size_t ws_bytes, void *stream);
 
 /* Number of (b, h) groups fa_forward_host pipelines (fewer if B*H is smaller). */
-#define FA_HOST_CHUNKS 4
+#define FA_HOST_CHUNKS 16
 
 /*
  * Device workspace bytes fa_forward_host needs for this shape (device copies of
