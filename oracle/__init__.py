@@ -42,10 +42,12 @@ def lib():
         L.oracle_online_rows.argtypes = common + [i64, i32, i64p, i64, dblp, dblp, i32]
         L.oracle_split_rows.argtypes = common + [i64p, i64, i64p, i64, dblp, dblp, i32]
         L.oracle_combine.argtypes = [i64, i64, i64, dblp, dblp, dblp, dblp]
+        L.oracle_attention_masked.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64,
+                                              ctypes.POINTER(ctypes.c_uint8), f32, dblp, dblp, i32]
         L.oracle_max_threads.argtypes = []
         for f in (L.oracle_attention_rows, L.oracle_attention, L.oracle_probs_row,
                   L.oracle_online_rows, L.oracle_split_rows, L.oracle_max_threads,
-                  L.oracle_combine):
+                  L.oracle_combine, L.oracle_attention_masked):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -176,4 +178,20 @@ def combine(o_parts, lse_parts):
     return o, lse
 
 
-__all__ = ["attention", "probs_row", "online", "split", "combine", "max_threads", "lib"]
+def attention_masked(q, k, v, visible, scale: float, threads: int = 0):
+    """Definition with an explicit mask: visible [B, Sq, Sk] (nonzero = key enters the row)."""
+    B, H, Sq, Sk, d = _dims(q, k, v)
+    vis = np.ascontiguousarray(np.asarray(visible, dtype=np.uint8).reshape(B, Sq, Sk))
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    o = np.empty((B, H, Sq, d), dtype=np.float64)
+    lse = np.empty((B, H, Sq), dtype=np.float64)
+    _check(lib().oracle_attention_masked(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                         _ptr(vb, ctypes.c_uint16), B, H, Sq, Sk, d,
+                                         _ptr(vis, ctypes.c_uint8), ctypes.c_float(scale),
+                                         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                         int(threads)), "attention_masked")
+    return o, lse
+
+
+__all__ = ["attention", "attention_masked", "probs_row", "online", "split", "combine",
+           "max_threads", "lib"]

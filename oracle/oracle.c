@@ -523,3 +523,83 @@ int oracle_combine(int64_t n_parts, int64_t n_rows, int64_t d, const double *o_p
     }
     return 0;
 }
+
+/*
+ * The definition with an explicit visibility mask instead of the causal rule:
+ * "Warmup Guide — Inference Optimization at Depth", Chapter 4 applies a mask
+ * to S before the softmax; here visible[(b * Sq + i) * Sk + j] != 0 means key
+ * j enters row i of batch element b (for every head). This covers the
+ * tree-structured verify step of "Lecture 06 — Making Decode Fast", section 3
+ * (several candidate continuations verified in one pass, each seeing the
+ * cache and its own ancestors), where the visible keys of a row are not a
+ * prefix. Rows with no visible key: o = 0, lse = -inf.
+ * o: [B,H,Sq,d], lse: [B,H,Sq].
+ */
+int oracle_attention_masked(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B,
+                            int64_t H, int64_t Sq, int64_t Sk, int64_t d, const uint8_t *visible,
+                            float scale, double *o, double *lse, int nthreads)
+{
+    int rc = check_args(q, k, v, B, H, Sq, Sk, d);
+    if (rc)
+        return rc;
+    if (!visible || !o || !lse)
+        return -1;
+    set_threads(nthreads);
+    const double sc = (double)scale;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)Sk);
+        int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (size_t)Sk);
+        if (!s || !idx) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < B * H * Sq; ++r) {
+            if (!s || !idx)
+                continue;
+            const int64_t b = r / (H * Sq), h = (r / Sq) % H, i = r % Sq;
+            const uint16_t *qi = q + r * d;
+            const uint16_t *kbh = k + (b * H + h) * Sk * d;
+            const uint16_t *vbh = v + (b * H + h) * Sk * d;
+            const uint8_t *vis = visible + (b * Sq + i) * Sk;
+            double *orow = o + r * d;
+            int64_t n = 0;
+            for (int64_t j = 0; j < Sk; ++j)
+                if (vis[j])
+                    idx[n++] = j;
+            for (int64_t t = 0; t < d; ++t)
+                orow[t] = 0.0;
+            if (n == 0) {
+                lse[r] = -INFINITY;
+                continue;
+            }
+            /* scores of the visible keys, then the two-pass safe softmax */
+            for (int64_t a = 0; a < n; ++a) {
+                const uint16_t *kj = kbh + idx[a] * d;
+                double dot = 0.0;
+                for (int64_t t = 0; t < d; ++t)
+                    dot += bf16_to_double(qi[t]) * bf16_to_double(kj[t]);
+                s[a] = sc * dot;
+            }
+            double m = -INFINITY;
+            for (int64_t a = 0; a < n; ++a)
+                if (s[a] > m)
+                    m = s[a];
+            double l = 0.0;
+            for (int64_t a = 0; a < n; ++a)
+                l += exp(s[a] - m);
+            for (int64_t a = 0; a < n; ++a) {
+                const double pj = exp(s[a] - m) / l;
+                const uint16_t *vj = vbh + idx[a] * d;
+                for (int64_t t = 0; t < d; ++t)
+                    orow[t] += pj * bf16_to_double(vj[t]);
+            }
+            lse[r] = m + log(l);
+        }
+        free(s);
+        free(idx);
+    }
+    return failed ? -4 : 0;
+}

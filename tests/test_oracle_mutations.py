@@ -34,6 +34,9 @@ MUTATIONS = {
     "online_form2_sum_uncorrected": ("        l = l * c_old + lb * c_blk;", "        l = l + lb * c_blk;"),
     "split_weights_unnormalised": ("                double w = exp(part_lse[c] - L);",
                                    "                double w = exp(part_lse[c] - M);"),
+    "masked_ignores_mask": ("                if (vis[j])\n                    idx[n++] = j;",
+                            "                if (vis[j] || 1)\n                    idx[n++] = j;"),
+    "masked_drops_scale": ("                s[a] = sc * dot;", "                s[a] = dot;"),
     "combine_weights_unnormalised": ("            double w = exp(lse_parts[c * n_rows + r] - L);",
                                      "            double w = exp(lse_parts[c * n_rows + r] - M);"),
 }

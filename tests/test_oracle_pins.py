@@ -182,6 +182,47 @@ def test_combine_of_separately_computed_parts_equals_unsplit():
     assert np.array_equal(o2, o_a.reshape(-1, 16)) and np.array_equal(l2, l_a.reshape(-1))
 
 
+def _causal_visible(B, Sq, Sk):
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    return np.broadcast_to(j <= i + (Sk - Sq), (B, Sq, Sk)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_masked_definition_reduces_to_causal_and_full(shape):
+    """An all-ones mask is non-causal attention; the bottom-right triangle is causal."""
+    B, H, Sq, Sk, d, causal = shape
+    w, q, k, v = case(B, H, Sq, Sk, d, causal, seed=47, factor=2.0)
+    o_full, l_full = oracle.attention(q, k, v, False, w.scale)
+    o, l = oracle.attention_masked(q, k, v, np.ones((B, Sq, Sk), np.uint8), w.scale)
+    assert np.max(np.abs(o - o_full)) < TOL and np.max(np.abs(l - l_full)) < TOL
+    o_c, l_c = oracle.attention(q, k, v, True, w.scale)
+    o, l = oracle.attention_masked(q, k, v, _causal_visible(B, Sq, Sk), w.scale)
+    assert np.max(np.abs(o - o_c)) < TOL
+    fin = np.isfinite(l_c)
+    assert np.array_equal(fin, np.isfinite(l)) and np.max(np.abs(l[fin] - l_c[fin])) < TOL
+
+
+def test_masked_definition_single_key_and_subset_equivalence():
+    """A row that sees one key returns its value row; a row that sees a key subset equals
+    plain attention over that subset of keys (a gather of K and V)."""
+    w, q, k, v = case(2, 2, 4, 12, 16, False, seed=53, factor=3.0)
+    vis = np.zeros((2, 4, 12), np.uint8)
+    vis[:, 0, 7] = 1                               # row 0: key 7 only
+    vis[:, 1, [0, 3, 5, 11]] = 1                   # row 1: a scattered subset
+    vis[:, 2, :] = 1                               # row 2: everything
+    o, l = oracle.attention_masked(q, k, v, vis, w.scale)   # row 3: nothing
+    vd = to_f64(v)
+    assert np.all(o[:, :, 0] == vd[:, :, 7])
+    sub = [0, 3, 5, 11]
+    o_s, l_s = oracle.attention(q[:, :, 1:2], k[:, :, sub], v[:, :, sub], False, w.scale)
+    assert np.max(np.abs(o[:, :, 1] - o_s[:, :, 0])) < TOL
+    assert np.max(np.abs(l[:, :, 1] - l_s[:, :, 0])) < TOL
+    o_f, l_f = oracle.attention(q[:, :, 2:3], k, v, False, w.scale)
+    assert np.max(np.abs(o[:, :, 2] - o_f[:, :, 0])) < TOL
+    assert np.all(o[:, :, 3] == 0) and np.all(np.isneginf(l[:, :, 3]))
+
+
 def test_key_value_permutation_invariance():
     """Non-causal attention is a function of the set of (key, value) pairs."""
     w, q, k, v = case(1, 2, 9, 40, 16, False, seed=29)
