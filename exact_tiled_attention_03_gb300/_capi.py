@@ -38,6 +38,8 @@ SIGNATURES = {
     "fa_verify_auto_splits": (_I32, [_I64] * 5),
     "fa_verify_forward_static": (_I32, _ATTN + [_I32, _P]),
     "fa_forward_host": (_I32, _ATTN + [_P, _SZ, _P]),
+    "fa_verify_tree_forward": (_I32, [_P] * 5 + [_I64] * 5 + [_P, _F32, _I32, _P, _SZ, _P]),
+    "fa_verify_paged_forward": (_I32, [_P] * 7 + [_I64] * 8 + [_I32, _P, _F32, _I32, _P, _SZ, _P]),
     "fa_forward_host_workspace_size": (_SZ, [_I64] * 5),
     "fa_status_string": (ctypes.c_char_p, [_I32]),
     "fa_device_status": (_I32, [_P]),
@@ -135,6 +137,23 @@ def fa_verify_forward_static(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, n_
     return load().fa_verify_forward_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
                                            Sq, Sk, d, int(bool(causal)), float(scale),
                                            int(n_split), _stream(stream))
+
+
+def fa_verify_tree_forward(q, k, v, o, lse, B, H, Sq, Sk, d, tree_mask, scale, n_split, workspace,
+                           ws_bytes, stream=None) -> int:
+    return load().fa_verify_tree_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq,
+                                         Sk, d, _ptr(tree_mask), float(scale), int(n_split),
+                                         _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def fa_verify_paged_forward(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, H, Sq, d,
+                            num_pages, page_size, max_pages_per_seq, max_seq_len, causal,
+                            tree_mask, scale, n_split, workspace, ws_bytes, stream=None) -> int:
+    return load().fa_verify_paged_forward(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(o),
+        _ptr(lse), B, H, Sq, d, num_pages, page_size, max_pages_per_seq, max_seq_len,
+        int(bool(causal)), _ptr(tree_mask), float(scale), int(n_split), _ptr(workspace),
+        int(ws_bytes), _stream(stream))
 
 
 def fa_forward_host(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, workspace=None, ws_bytes=0,

@@ -225,6 +225,21 @@ bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uin
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                         uint64_t mid, uint64_t outer, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[4] = {inner, rows, mid, outer};
+    const cuuint64_t strides[3] = {inner * 2, inner * rows * 2, inner * rows * mid * 2};
+    const cuuint32_t box[4] = {64, box_rows, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -308,6 +323,90 @@ fa_status_t fa_verify_forward(const void *q, const void *k, const void *v, void 
     return launch_verify(
         make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream, di->status), ns,
         workspace, ws_bytes);
+}
+
+fa_status_t fa_verify_tree_forward(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                   int64_t d, const uint32_t *tree_mask, float scale, int n_split,
+                                   void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!tree_mask || (reinterpret_cast<uintptr_t>(tree_mask) & 3u) != 0)
+        return FA_ERR_INVALID_ARG;
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    if (Sq > FA_VERIFY_MAX_SQ || B * H > 65535)
+        return FA_ERR_UNSUPPORTED;
+    const int64_t max_split = (Sk + kVerifyStageKeys - 1) / kVerifyStageKeys;
+    if (n_split < 0 || n_split > max_split || n_split > 65535)
+        return FA_ERR_INVALID_ARG;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    const int ns = verify_splits_or_auto(n_split, B * H, Sk, di);
+    const size_t need = verify_workspace_bytes(B * H, Sq, d, ns);
+    if (need > 0 && (!workspace || ws_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return FA_ERR_WORKSPACE;
+    VerifyOptions opt;
+    opt.tree_mask = tree_mask;
+    return launch_verify(
+        make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, 1, scale, stream, di->status), ns,
+        workspace, ws_bytes, opt);
+}
+
+fa_status_t fa_verify_paged_forward(const void *q, const void *k_pages, const void *v_pages,
+                                    const int32_t *block_table, const int32_t *seq_lens, void *o,
+                                    float *lse, int64_t B, int64_t H, int64_t Sq, int64_t d,
+                                    int64_t num_pages, int64_t page_size,
+                                    int64_t max_pages_per_seq, int64_t max_seq_len, int causal,
+                                    const uint32_t *tree_mask, float scale, int n_split,
+                                    void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!block_table || !seq_lens)
+        return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0 ||
+        (tree_mask && (reinterpret_cast<uintptr_t>(tree_mask) & 3u) != 0))
+        return FA_ERR_INVALID_ARG;
+    if (num_pages < 1 || max_pages_per_seq < 1 || page_size < 1 || max_seq_len < 1)
+        return FA_ERR_INVALID_ARG;
+    const bool page_ok = page_size % 16 == 0 &&
+                         (page_size < kVerifyStageKeys ? kVerifyStageKeys % page_size == 0
+                                                       : page_size % kVerifyStageKeys == 0);
+    if (!page_ok)
+        return FA_ERR_UNSUPPORTED;
+    const int64_t lim31 = (int64_t(1) << 31) - 1;
+    if (num_pages > lim31 || max_pages_per_seq > lim31 / page_size ||
+        max_seq_len > max_pages_per_seq * page_size)
+        return FA_ERR_INVALID_ARG;
+    // Validate shapes and pointers with the pool standing in for K/V.
+    fa_status_t st = validate(q, k_pages, v_pages, o, lse, B, H, Sq, max_seq_len, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    if (Sq > FA_VERIFY_MAX_SQ || B * H > 65535)
+        return FA_ERR_UNSUPPORTED;
+    const int64_t max_split = (max_seq_len + kVerifyStageKeys - 1) / kVerifyStageKeys;
+    if (n_split < 0 || n_split > max_split || n_split > 65535)
+        return FA_ERR_INVALID_ARG;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    const int ns = verify_splits_or_auto(n_split, B * H, max_seq_len, di);
+    const size_t need = verify_workspace_bytes(B * H, Sq, d, ns);
+    if (need > 0 && (!workspace || ws_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return FA_ERR_WORKSPACE;
+    VerifyOptions opt;
+    opt.tree_mask = tree_mask;
+    opt.block_table = block_table;
+    opt.seq_lens = seq_lens;
+    opt.page_size = page_size;
+    opt.num_pages = num_pages;
+    opt.max_pages = max_pages_per_seq;
+    return launch_verify(make_problem(q, k_pages, v_pages, o, lse, B, H, Sq, max_seq_len, d,
+                                      causal, scale, stream, di->status),
+                         ns, workspace, ws_bytes, opt);
 }
 
 size_t fa_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d)

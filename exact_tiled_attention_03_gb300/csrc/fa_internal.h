@@ -28,10 +28,26 @@ struct Problem {
 bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                          uint64_t depth, uint32_t box_rows);
 
+// Row-major [outer, mid, rows, inner] bf16 tensor as a 4-D TMA map with a
+// (64 x box_rows x 1 x 1) box and 128-byte swizzle (K/V page pools).
+bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                         uint64_t mid, uint64_t outer, uint32_t box_rows);
+
+// Options of the split-KV path beyond the contiguous causal/non-causal case.
+struct VerifyOptions {
+    const uint32_t *tree_mask = nullptr;  // [B, Sq] draft-position masks (replaces causal)
+    // Paged K/V: Problem::k / v are page pools [num_pages, H, page_size, d],
+    // Problem::Sk is the longest sequence.
+    const int32_t *block_table = nullptr;  // [B, max_pages]
+    const int32_t *seq_lens = nullptr;     // [B]
+    int64_t page_size = 0, num_pages = 0, max_pages = 0;
+};
+
 // Launchers. Each validates nothing (fa_abi.cu does) and returns FA_OK or
 // FA_ERR_CUDA.
 fa_status_t launch_prefill_sm103(const Problem &p);
-fa_status_t launch_verify(const Problem &p, int n_split, void *workspace, size_t ws_bytes);
+fa_status_t launch_verify(const Problem &p, int n_split, void *workspace, size_t ws_bytes,
+                          const VerifyOptions &opt = VerifyOptions());
 fa_status_t launch_reference_simt(const Problem &p);
 fa_status_t launch_selftest_umma(const void *a, const void *b, float *c, int n, int k,
                                  int b_mn_major, cudaStream_t stream, unsigned int *status);

@@ -21,6 +21,15 @@
 //       O   = sum_s exp(LSE_s - LSE) O_s,
 //     the chunk-level form of Chapter 3's update (the pages give no formula
 //     for the "final combine"; this is the one the update implies).
+// Which keys a query row sees is a bitmask over the last Sq key positions
+// (the draft positions; every key before them is visible): bits 0..i for the
+// causal chain, every bit for non-causal, or a caller-given tree mask, where
+// each candidate sees the cache and its own ancestors (tree-attention over a
+// draft tree, "Lecture 06", section 3). K/V can come from a contiguous
+// [B, H, Sk, d] tensor or from page pools through a block table with a
+// length per sequence ("Warmup Guide", Chapter 8 and its Q&A: the kernel
+// walks the block table once per tile); each 64-key stage is then one TMA box
+// per page it spans.
 // This shape moves ~5 flops per byte: it is bound by HBM, so the legacy
 // warp-level MMA is ample; what matters is keeping enough bytes in flight.
 #include <cmath>
@@ -52,10 +61,14 @@ struct Cfg {
 };
 
 struct Params {
-    int Sq, Sk, BH, n_split;
+    int Sq, Sk, BH, H, n_split;
     int chunk;  // keys per split (multiple of kStageKeys)
-    int causal;
+    int mode;   // 0: every draft position, 1: causal chain, 2: tree_mask
     float scale, scale_log2;
+    const uint32_t *tree_mask;   // [B, Sq] (mode 2)
+    const int32_t *seq_lens;     // [B] keys per sequence (paged); nullptr: Sk for all
+    const int32_t *block_table;  // [B, max_pages] physical page of each logical page (paged)
+    int page_size, max_pages, num_pages;
     const __nv_bfloat16 *q;
     __nv_bfloat16 *o;   // final output (used when n_split == 1)
     float *lse;         // final LSE (used when n_split == 1)
@@ -70,12 +83,24 @@ struct Bars {
     int abort_flag;
 };
 
-__device__ __forceinline__ int visible_keys(int i, int Sq, int Sk, int causal)
+// Bitmask over the Sq draft positions that row i sees.
+__device__ __forceinline__ uint32_t draft_mask(const Params &p, int b, int i)
 {
-    if (!causal)
-        return Sk;
-    int n = i + (Sk - Sq) + 1;
-    return n < 0 ? 0 : (n > Sk ? Sk : n);
+    if (i >= p.Sq)
+        return 0u;
+    const uint32_t all = p.Sq >= 32 ? ~0u : ((1u << p.Sq) - 1u);
+    if (p.mode == 0)
+        return all;
+    if (p.mode == 1)
+        return i >= 31 ? ~0u : ((2u << i) - 1u);
+    return p.tree_mask[static_cast<size_t>(b) * p.Sq + i] & all;
+}
+
+// Key j (logical) is visible through mask `rm`: everything before the draft
+// positions, and draft position j - prefix when its bit is set.
+__device__ __forceinline__ bool key_visible(int j, int prefix, int Sk_b, uint32_t rm)
+{
+    return j < prefix || (j < Sk_b && ((rm >> (j - prefix)) & 1u));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
@@ -110,7 +135,7 @@ __device__ __forceinline__ uint32_t ld_bf16x2_or_zero(const __nv_bfloat16 *p, bo
     return valid ? *reinterpret_cast<const uint32_t *>(p) : 0u;
 }
 
-template <int D>
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_verify_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const Params p)
@@ -125,10 +150,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int split = blockIdx.x;
     const int bh = blockIdx.y;
 
-    // Keys this CTA covers: its chunk, cut at the last key any row may see.
-    const int lim_max = visible_keys(p.Sq - 1, p.Sq, p.Sk, p.causal);
+    const int b = bh / p.H, h = bh % p.H;
+    // Keys of this sequence; the draft positions are its last Sq keys.
+    int Sk_b = p.Sk;
+    if (kPaged && p.seq_lens) {
+        Sk_b = p.seq_lens[b];
+        Sk_b = Sk_b < 0 ? 0 : min(Sk_b, p.max_pages * p.page_size);
+    }
+    const int prefix = Sk_b - p.Sq;
+    // Keys this CTA covers: its chunk of the sequence.
     const int kv_begin = split * p.chunk;
-    const int kv_end = min(kv_begin + p.chunk, lim_max);
+    const int kv_end = min(kv_begin + p.chunk, Sk_b);
     const int n_st = kv_end > kv_begin ? (kv_end - kv_begin + kStageKeys - 1) / kStageKeys : 0;
 
     if (threadIdx.x == 0) {
@@ -143,27 +175,73 @@ __global__ void __launch_bounds__(kThreads, 2)
     int *abort_flag = &bars->abort_flag;
 
     if (warp == kProducerWarp) {
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();  // K/V are streamed once
-            int st = 0;
-            for (; st < n_st; ++st) {
-                const int s = st % C::kStages;
-                const uint32_t use = st / C::kStages;
-                if (use > 0 && !mbar_wait(&bars->empty[s], (use - 1) & 1, abort_flag, p.status))
-                    break;
+        // The whole warp walks the stages (it shares the block-table reads);
+        // lane 0 issues the copies.
+        const uint64_t pol = l2_policy_evict_first();  // K/V are streamed once
+        const int P = p.page_size;
+        const int n_pages_b = kPaged ? (Sk_b + P - 1) / P : 0;
+        int cached = -1, my_page = 0;
+        // Physical page of logical page lp (warp-collective): 32 entries of the
+        // block table are read at a time, one per lane. Pages past the
+        // sequence get an out-of-range index, which TMA fills with zeros.
+        auto page_of = [&](int lp) {
+            const int base = lp & ~31;
+            if (base != cached) {
+                cached = base;
+                const int idx = base + lane;
+                my_page = idx < n_pages_b
+                              ? p.block_table[static_cast<size_t>(b) * p.max_pages + idx]
+                              : p.num_pages;
+            }
+            return __shfl_sync(0xffffffffu, my_page, lp & 31);
+        };
+        int st = 0;
+        for (; st < n_st; ++st) {
+            const int s = st % C::kStages;
+            const uint32_t use = st / C::kStages;
+            if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], (use - 1) & 1,
+                                                               abort_flag, p.status)))
+                break;
+            if (lane == 0)
                 mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
-                uint8_t *dst = smem + s * C::kStageBytes;
-                const int key = kv_begin + st * kStageKeys;
-                for (int b = 0; b < C::kBoxes; ++b) {
-                    tma_load_3d_hint(dst + b * kBoxBytes, &tm_k, &bars->full[s], b * 64, key, bh,
-                                     pol);
-                    tma_load_3d_hint(dst + C::kTileBytes + b * kBoxBytes, &tm_v, &bars->full[s],
-                                     b * 64, key, bh, pol);
+            uint8_t *dst = smem + s * C::kStageBytes;
+            const int key = kv_begin + st * kStageKeys;
+            if constexpr (!kPaged) {
+                if (lane == 0)
+                    for (int q = 0; q < C::kBoxes; ++q) {
+                        tma_load_3d_hint(dst + q * kBoxBytes, &tm_k, &bars->full[s], q * 64, key,
+                                         bh, pol);
+                        tma_load_3d_hint(dst + C::kTileBytes + q * kBoxBytes, &tm_v,
+                                         &bars->full[s], q * 64, key, bh, pol);
+                    }
+            } else if (P >= kStageKeys) {
+                const int pid = page_of(key / P);
+                if (lane == 0)
+                    for (int q = 0; q < C::kBoxes; ++q) {
+                        tma_load_4d_hint(dst + q * kBoxBytes, &tm_k, &bars->full[s], q * 64,
+                                         key % P, h, pid, pol);
+                        tma_load_4d_hint(dst + C::kTileBytes + q * kBoxBytes, &tm_v,
+                                         &bars->full[s], q * 64, key % P, h, pid, pol);
+                    }
+            } else {
+                // The stage spans kStageKeys / P pages: one box of P rows each,
+                // placed at consecutive rows of the stage (P * 128 bytes is a
+                // multiple of the 1024-byte swizzle atom).
+                for (int sub = 0; sub < kStageKeys / P; ++sub) {
+                    const int pid = page_of(key / P + sub);
+                    if (lane == 0)
+                        for (int q = 0; q < C::kBoxes; ++q) {
+                            tma_load_4d_hint(dst + q * kBoxBytes + sub * P * 128, &tm_k,
+                                             &bars->full[s], q * 64, 0, h, pid, pol);
+                            tma_load_4d_hint(dst + C::kTileBytes + q * kBoxBytes + sub * P * 128,
+                                             &tm_v, &bars->full[s], q * 64, 0, h, pid, pol);
+                        }
                 }
             }
+        }
+        if (lane == 0)
             for (int k = max(0, st - C::kStages); k < st; ++k)
                 mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status);
-        }
         // Match the consumers' two block barriers (ring -> scratch, scratch ready).
         __syncthreads();
         __syncthreads();
@@ -186,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         qa[kk][2] = ld_bf16x2_or_zero(qb + g * D + c + 8, g < p.Sq);
         qa[kk][3] = ld_bf16x2_or_zero(qb + (g + 8) * D + c + 8, g + 8 < p.Sq);
     }
-    const int lim0 = visible_keys(g, p.Sq, p.Sk, p.causal);
-    const int lim1 = visible_keys(g + 8, p.Sq, p.Sk, p.causal);
+    const uint32_t rm0 = draft_mask(p, b, g), rm1 = draft_mask(p, b, g + 8);
 
     float o[D / 8][4];
 #pragma unroll
@@ -223,18 +300,22 @@ __global__ void __launch_bounds__(kThreads, 2)
             mma_bf16_16816(sc[0], qa[kk], b0, b1);
             mma_bf16_16816(sc[1], qa[kk], b2, b3);
         }
-        // Mask and online softmax over this warp's 16 keys.
-        const int key_base = kv_begin + st * kStageKeys + warp * 16 + 2 * tq;
+        // Mask (only stages that reach the draft positions or past the end)
+        // and online softmax over this warp's 16 keys.
+        const int stage_key = kv_begin + st * kStageKeys;
+        if (stage_key + kStageKeys > prefix) {
+            const int key_base = stage_key + warp * 16 + 2 * tq;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int key = key_base + nt * 8 + e;
-                if (key >= lim0)
-                    sc[nt][e] = -INFINITY;
-                if (key >= lim1)
-                    sc[nt][2 + e] = -INFINITY;
-            }
+                for (int e = 0; e < 2; ++e) {
+                    const int key = key_base + nt * 8 + e;
+                    if (!key_visible(key, prefix, Sk_b, rm0))
+                        sc[nt][e] = -INFINITY;
+                    if (!key_visible(key, prefix, Sk_b, rm1))
+                        sc[nt][2 + e] = -INFINITY;
+                }
+        }
         float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
         float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -383,23 +464,40 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int D>
-fa_status_t launch(const Problem &pr, int n_split, void *ws, size_t ws_bytes)
+fa_status_t launch(const Problem &pr, int n_split, void *ws, size_t ws_bytes,
+                   const VerifyOptions &opt)
 {
     using C = Cfg<D>;
     const int64_t BH = pr.B * pr.H;
+    const bool paged = opt.block_table != nullptr;
     CUtensorMap tk, tv;
-    if (!encode_tmap_bf16_3d(&tk, pr.k, D, pr.Sk, BH, kStageKeys) ||
-        !encode_tmap_bf16_3d(&tv, pr.v, D, pr.Sk, BH, kStageKeys))
-        return FA_ERR_CUDA;
+    if (!paged) {
+        if (!encode_tmap_bf16_3d(&tk, pr.k, D, pr.Sk, BH, kStageKeys) ||
+            !encode_tmap_bf16_3d(&tv, pr.v, D, pr.Sk, BH, kStageKeys))
+            return FA_ERR_CUDA;
+    } else {
+        const uint32_t box_rows =
+            static_cast<uint32_t>(opt.page_size < kStageKeys ? opt.page_size : kStageKeys);
+        if (!encode_tmap_bf16_4d(&tk, pr.k, D, opt.page_size, pr.H, opt.num_pages, box_rows) ||
+            !encode_tmap_bf16_4d(&tv, pr.v, D, opt.page_size, pr.H, opt.num_pages, box_rows))
+            return FA_ERR_CUDA;
+    }
     Params p;
     p.Sq = static_cast<int>(pr.Sq);
     p.Sk = static_cast<int>(pr.Sk);
     p.BH = static_cast<int>(BH);
+    p.H = static_cast<int>(pr.H);
     p.n_split = n_split;
     p.chunk = static_cast<int>(verify_chunk_keys(pr.Sk, n_split));
-    p.causal = pr.causal ? 1 : 0;
+    p.mode = opt.tree_mask ? 2 : (pr.causal ? 1 : 0);
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.tree_mask = opt.tree_mask;
+    p.seq_lens = opt.seq_lens;
+    p.block_table = opt.block_table;
+    p.page_size = static_cast<int>(opt.page_size);
+    p.max_pages = static_cast<int>(opt.max_pages);
+    p.num_pages = static_cast<int>(opt.num_pages);
     p.q = static_cast<const __nv_bfloat16 *>(pr.q);
     p.o = static_cast<__nv_bfloat16 *>(pr.o);
     p.lse = pr.lse;
@@ -414,12 +512,12 @@ fa_status_t launch(const Problem &pr, int n_split, void *ws, size_t ws_bytes)
         p.ws_o = static_cast<float *>(ws);
         p.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + o_bytes);
     }
-    auto kern = fa_verify_split_kernel<D>;
+    if (BH > 65535)
+        return FA_ERR_UNSUPPORTED;
+    auto kern = paged ? fa_verify_split_kernel<D, true> : fa_verify_split_kernel<D, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return FA_ERR_CUDA;
-    if (BH > 65535)
-        return FA_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(n_split), static_cast<unsigned>(BH));
     kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(tk, tv, p);
     if (cudaGetLastError() != cudaSuccess)
@@ -475,12 +573,13 @@ int verify_auto_splits(int64_t BH, int64_t Sk, int num_sms)
     return best;
 }
 
-fa_status_t launch_verify(const Problem &p, int n_split, void *workspace, size_t ws_bytes)
+fa_status_t launch_verify(const Problem &p, int n_split, void *workspace, size_t ws_bytes,
+                          const VerifyOptions &opt)
 {
     if (p.d == 128)
-        return verify::launch<128>(p, n_split, workspace, ws_bytes);
+        return verify::launch<128>(p, n_split, workspace, ws_bytes, opt);
     if (p.d == 64)
-        return verify::launch<64>(p, n_split, workspace, ws_bytes);
+        return verify::launch<64>(p, n_split, workspace, ws_bytes, opt);
     return FA_ERR_UNSUPPORTED;
 }
 

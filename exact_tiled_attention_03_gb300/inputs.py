@@ -166,3 +166,46 @@ def sample_rows(w: Workload, per_head: int | None = None, n_total: int | None = 
 
 def with_seed(w: Workload, seed: int) -> Workload:
     return replace(w, seed=seed)
+
+
+def make_tree_masks(B: int, Sq: int, seed: int = 0):
+    """Seeded random draft trees, one per sequence, as uint32 [B, Sq] masks.
+
+    Candidate 0 is the root; candidate i > 0 hangs under a random earlier
+    candidate. Bit k of mask[b][i] is set when candidate k is an ancestor of
+    candidate i or i itself (what tree-attention lets it see among the drafts).
+    """
+    g = torch.Generator().manual_seed(seed)
+    masks = torch.zeros((B, Sq), dtype=torch.int64)
+    for b in range(B):
+        for i in range(Sq):
+            parent = int(torch.randint(0, i, (1,), generator=g)) if i > 0 else -1
+            masks[b, i] = (1 << i) | (int(masks[b, parent]) if parent >= 0 else 0)
+    return masks.to(torch.int32)   # bit patterns; Sq <= 31
+
+
+def make_paged_kv(k: torch.Tensor, v: torch.Tensor, seq_lens, page_size: int,
+                  extra_pages: int = 3, seed: int = 0):
+    """Scatter contiguous K, V [B, H, Sk, d] into page pools [num_pages, H, page_size, d]
+    through a seeded random block table. Keys past seq_lens[b] are not stored.
+    Returns (k_pages, v_pages, block_table int32 [B, max_pages], seq_lens int32 [B])."""
+    B, H, Sk, d = k.shape
+    max_pages = -(-Sk // page_size)
+    need = sum(-(-int(n) // page_size) for n in seq_lens)
+    num_pages = need + extra_pages
+    g = torch.Generator().manual_seed(seed)
+    order = torch.randperm(num_pages, generator=g)
+    k_pages = torch.randn((num_pages, H, page_size, d), generator=g).to(k.dtype)
+    v_pages = torch.randn((num_pages, H, page_size, d), generator=g).to(v.dtype)
+    table = torch.full((B, max_pages), -7, dtype=torch.int32)   # unused entries: garbage
+    nxt = 0
+    for b in range(B):
+        for lp in range(-(-int(seq_lens[b]) // page_size)):
+            phys = int(order[nxt])
+            nxt += 1
+            table[b, lp] = phys
+            lo, hi = lp * page_size, min((lp + 1) * page_size, int(seq_lens[b]))
+            k_pages[phys, :, : hi - lo] = k[b, :, lo:hi]
+            v_pages[phys, :, : hi - lo] = v[b, :, lo:hi]
+    return k_pages, v_pages, table, torch.tensor(list(seq_lens), dtype=torch.int32)
+

@@ -143,6 +143,56 @@ size_t fa_verify_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, in
 int fa_verify_auto_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
 
 /*
+ * Split-KV verify with a tree of draft tokens: the Sq queries are candidate
+ * tokens of a draft tree appended after Sk - Sq cached keys; each candidate
+ * attends to the whole cache and to the candidates its tree mask selects
+ * (normally its ancestors and itself), so several continuations are verified
+ * in one pass ("Lecture 06 — Making Decode Fast", section 3: tree-attention
+ * over a draft tree).
+ *   tree_mask : device uint32 [B, Sq]; bit k of tree_mask[b][i] set means
+ *               query i of sequence b sees key Sk - Sq + k (bits >= Sq are
+ *               ignored). A chain (bits 0..i) is the causal case.
+ * Other arguments as fa_verify_forward (causal is replaced by the mask).
+ * Returns FA_ERR_INVALID_ARG for a NULL or misaligned tree_mask.
+ */
+fa_status_t fa_verify_tree_forward(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                   int64_t d, const uint32_t *tree_mask, float scale, int n_split,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Split-KV verify reading K and V through a block table (paged KV cache,
+ * "Warmup Guide — Inference Optimization at Depth", Chapter 8 and its Q&A:
+ * the kernel walks the block table once per tile). Sequences may have
+ * different lengths.
+ *   k_pages, v_pages : device bf16 [num_pages, H, page_size, d] page pools.
+ *   block_table      : device int32 [B, max_pages_per_seq]; entry p of row b
+ *                      is the pool page holding keys [p*page_size,
+ *                      (p+1)*page_size) of sequence b. Entries past a
+ *                      sequence's length are not read.
+ *   seq_lens         : device int32 [B], the keys of each sequence; values are
+ *                      clamped to [0, max_pages_per_seq * page_size]. A
+ *                      sequence's last Sq keys are its draft positions.
+ *   page_size        : 16, 32, or a multiple of 64 (one TMA box per page per
+ *                      64-key stage, or per page when pages are smaller).
+ *   max_seq_len      : host value, >= every seq_lens entry and
+ *                      <= max_pages_per_seq * page_size; sets the split size.
+ *   causal, tree_mask: bottom-right causal per sequence, or (tree_mask != NULL)
+ *                      the tree masks of fa_verify_tree_forward.
+ *   workspace        : fa_verify_workspace_size(B, H, Sq, max_seq_len, d,
+ *                      n_split) bytes when the split count exceeds one.
+ * A page index outside [0, num_pages) is read as zeros (it never faults).
+ * q, o, lse as fa_verify_forward.
+ */
+fa_status_t fa_verify_paged_forward(const void *q, const void *k_pages, const void *v_pages,
+                                    const int32_t *block_table, const int32_t *seq_lens, void *o,
+                                    float *lse, int64_t B, int64_t H, int64_t Sq, int64_t d,
+                                    int64_t num_pages, int64_t page_size,
+                                    int64_t max_pages_per_seq, int64_t max_seq_len, int causal,
+                                    const uint32_t *tree_mask, float scale, int n_split,
+                                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Attention forward on HOST-resident tensors, with the transfers inside the
  * call: the end-to-end form of fa_forward for a caller whose Q, K, V live in
  * host memory and who wants O and LSE back in host memory.

@@ -108,6 +108,29 @@ def test_workspace_size_is_zero_for_the_prefill_path(capi):
     assert n == o_bytes + l_bytes
 
 
+def test_tree_and_paged_entry_points_validate_first(capi):
+    A = ALIGNED
+    t = capi.fa_verify_tree_forward
+    assert t(A, A, A, A, A, 1, 1, 5, 100, 128, None, 0.1, 0, None, 0, 0) == capi.FA_ERR_INVALID_ARG
+    assert t(A, A, A, A, A, 1, 1, 5, 100, 128, A + 2, 0.1, 0, None, 0, 0) == capi.FA_ERR_INVALID_ARG
+    assert t(A, A, A, A, A, 1, 1, 17, 100, 128, A, 0.1, 0, None, 0, 0) == capi.FA_ERR_UNSUPPORTED
+    p = capi.fa_verify_paged_forward
+    ok = dict(B=2, H=2, Sq=5, d=128, num_pages=10, page_size=16, max_pages=8, max_len=100)
+    def call(**kw):
+        a = dict(ok, **kw)
+        return p(A, A, A, kw.get("table", A), kw.get("lens", A), A, A, a["B"], a["H"], a["Sq"],
+                 a["d"], a["num_pages"], a["page_size"], a["max_pages"], a["max_len"], 1, None,
+                 0.1, 0, None, 0, 0)
+    assert call(table=None) == capi.FA_ERR_INVALID_ARG
+    assert call(lens=None) == capi.FA_ERR_INVALID_ARG
+    assert call(page_size=24) == capi.FA_ERR_UNSUPPORTED
+    assert call(page_size=96) == capi.FA_ERR_UNSUPPORTED
+    assert call(max_len=129) == capi.FA_ERR_INVALID_ARG     # > max_pages * page_size
+    assert call(num_pages=0) == capi.FA_ERR_INVALID_ARG
+    assert call(Sq=17) == capi.FA_ERR_UNSUPPORTED
+    assert call(d=96) == capi.FA_ERR_UNSUPPORTED
+
+
 def test_host_entry_point_validates_first(capi):
     f = capi.fa_forward_host
     assert f(None, 1, 1, 1, 1, 1, 1, 256, 256, 128, 1, 0.1, None, 0, 0) == capi.FA_ERR_INVALID_ARG
