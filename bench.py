@@ -257,6 +257,62 @@ def run_reference(args, world, rank):
     return 0
 
 
+def measure_verify_variants(wv, device, sptr, args, peaks):
+    """GB/s of the verify workload as a draft tree (random trees over the 5
+    candidates) and read from a paged cache (random block table; page sizes
+    16 and 64), against the same algorithmic bytes as the contiguous form."""
+    from exact_tiled_attention_03_gb300 import _capi
+    from exact_tiled_attention_03_gb300.inputs import make_tree_masks
+
+    q, k, v = (t.to(device) for t in make_qkv(wv))
+    o = torch.empty_like(q)
+    lse = torch.empty((wv.B, wv.H, wv.Sq), dtype=torch.float32, device=device)
+    n_split = _capi.fa_verify_auto_splits(wv.B, wv.H, wv.Sq, wv.Sk, wv.d)
+    need = _capi.fa_verify_workspace_size(wv.B, wv.H, wv.Sq, wv.Sk, wv.d, n_split)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    masks = make_tree_masks(wv.B, wv.Sq, seed=wv.seed).to(device)
+    out = {}
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        n = max(10, args.steps)
+        per = time_steps(fn, n, torch.cuda.current_stream(device)) / n
+        gbs = wv.io_bytes() / per / 1e9
+        return {"us_per_step": per * 1e6, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+
+    def tree():
+        st = _capi.fa_verify_tree_forward(q, k, v, o, lse, wv.B, wv.H, wv.Sq, wv.Sk, wv.d, masks,
+                                          wv.scale, n_split, ws, need, sptr)
+        if st != 0:
+            raise _capi.FAError(st, "fa_verify_tree_forward")
+    out["tree"] = timed(tree)
+    for P in (16, 64):
+        n_lp = wv.Sk // P
+        g = torch.Generator(device=device).manual_seed(wv.seed + P)
+        perm = torch.randperm(wv.B * n_lp, generator=g, device=device)
+        pages_k = k.reshape(wv.B, wv.H, n_lp, P, wv.d).permute(0, 2, 1, 3, 4).reshape(-1, wv.H, P, wv.d)
+        pages_v = v.reshape(wv.B, wv.H, n_lp, P, wv.d).permute(0, 2, 1, 3, 4).reshape(-1, wv.H, P, wv.d)
+        kp = torch.empty_like(pages_k)
+        vp = torch.empty_like(pages_v)
+        kp[perm] = pages_k
+        vp[perm] = pages_v
+        table = perm.reshape(wv.B, n_lp).to(torch.int32).contiguous()
+        lens = torch.full((wv.B,), wv.Sk, dtype=torch.int32, device=device)
+
+        def paged():
+            st = _capi.fa_verify_paged_forward(q, kp, vp, table, lens, o, lse, wv.B, wv.H, wv.Sq,
+                                               wv.d, kp.shape[0], P, n_lp, wv.Sk, 1, None,
+                                               wv.scale, n_split, ws, need, sptr)
+            if st != 0:
+                raise _capi.FAError(st, "fa_verify_paged_forward")
+        out[f"paged_p{P}"] = timed(paged)
+        del kp, vp, pages_k, pages_v
+    torch.cuda.synchronize()
+    return out
+
+
+
 def config_block(w, world):
     return {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
             "causal": w.causal, "scale": w.scale, "parallelism": f"replicas x{world}",
@@ -370,6 +426,12 @@ def run_ours(args, world, rank, local):
                   "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, 1.0)}
         del qv, kv_, vv, ov, lv, ws
 
+    # the verify step's tree-mask and paged-cache forms, same bytes and roofline
+    verify_ext = None
+    if not args.no_verify:
+        verify_ext = measure_verify_variants(rank_workload(VERIFY, rank), device, sptr, args,
+                                             peaks)
+
     # the CPU oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -394,7 +456,8 @@ def run_ours(args, world, rank, local):
                          "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, 1.0)},
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
-            "e2e": e2e, "verify": verify, "cpu_baseline": cpu, "clocks": clocks,
+            "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "cpu_baseline": cpu,
+            "clocks": clocks,
             "gpu_launches": args.steps,  # one prefill kernel per timed step
             "gpu": torch.cuda.get_device_name(device),
         }
