@@ -42,12 +42,14 @@ def lib():
         L.oracle_online_rows.argtypes = common + [i64, i32, i64p, i64, dblp, dblp, i32]
         L.oracle_split_rows.argtypes = common + [i64p, i64, i64p, i64, dblp, dblp, i32]
         L.oracle_combine.argtypes = [i64, i64, i64, dblp, dblp, dblp, dblp]
+        L.oracle_attention_backward.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64,
+                                                i32, f32, dblp, dblp, dblp, i32]
         L.oracle_attention_masked.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64,
                                               ctypes.POINTER(ctypes.c_uint8), f32, dblp, dblp, i32]
         L.oracle_max_threads.argtypes = []
         for f in (L.oracle_attention_rows, L.oracle_attention, L.oracle_probs_row,
                   L.oracle_online_rows, L.oracle_split_rows, L.oracle_max_threads,
-                  L.oracle_combine, L.oracle_attention_masked):
+                  L.oracle_combine, L.oracle_attention_masked, L.oracle_attention_backward):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -193,5 +195,21 @@ def attention_masked(q, k, v, visible, scale: float, threads: int = 0):
     return o, lse
 
 
-__all__ = ["attention", "attention_masked", "probs_row", "online", "split", "combine",
+def attention_backward(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
+    """Gradients (dq, dk, dv) of the definition for upstream gradient dout, fp64."""
+    B, H, Sq, Sk, d = _dims(q, k, v)
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    dq = np.empty((B, H, Sq, d), dtype=np.float64)
+    dk = np.empty((B, H, Sk, d), dtype=np.float64)
+    dv = np.empty((B, H, Sk, d), dtype=np.float64)
+    _check(lib().oracle_attention_backward(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                           _ptr(vb, ctypes.c_uint16), _ptr(db, ctypes.c_uint16),
+                                           B, H, Sq, Sk, d, int(bool(causal)),
+                                           ctypes.c_float(scale), _ptr(dq, ctypes.c_double),
+                                           _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+                                           int(threads)), "attention_backward")
+    return dq, dk, dv
+
+
+__all__ = ["attention", "attention_backward", "attention_masked", "probs_row", "online", "split", "combine",
            "max_threads", "lib"]

@@ -603,3 +603,94 @@ int oracle_attention_masked(const uint16_t *q, const uint16_t *k, const uint16_t
     }
     return failed ? -4 : 0;
 }
+
+/*
+ * Gradients of the definition, given the upstream gradient dO: the backward
+ * pass the pages describe ("Warmup Guide — Inference Optimization at Depth",
+ * Chapter 4: recompute the probability tiles from Q and K instead of storing
+ * P). Here P is simply recomputed row by row from the definition (fp64), and
+ * the chain rule of O = softmax(scale * Q K^T + mask) V gives, per row i:
+ *   dP_ij = dO_i . v_j,       D_i = sum_j P_ij dP_ij,
+ *   dS_ij = P_ij (dP_ij - D_i),
+ *   dQ_i  = scale * sum_j dS_ij k_j,
+ *   dK_j += scale * dS_ij q_i,   dV_j += P_ij dO_i.
+ * q, k, v, dO: bf16 bits ([B,H,Sq,d], [B,H,Sk,d] x2, [B,H,Sq,d]); outputs
+ * dq [B,H,Sq,d], dk and dv [B,H,Sk,d] (doubles). Rows with no visible key
+ * contribute nothing.
+ */
+int oracle_attention_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const uint16_t *dout, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                              int64_t d, int causal, float scale, double *dq, double *dk,
+                              double *dv, int nthreads)
+{
+    int rc = check_args(q, k, v, B, H, Sq, Sk, d);
+    if (rc)
+        return rc;
+    if (!dout || !dq || !dk || !dv)
+        return -1;
+    set_threads(nthreads);
+    const double sc = (double)scale;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)Sk);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)Sk);
+        if (!p || !dp) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            if (!p || !dp)
+                continue;
+            const uint16_t *kbh = k + bh * Sk * d, *vbh = v + bh * Sk * d;
+            double *dkbh = dk + bh * Sk * d, *dvbh = dv + bh * Sk * d;
+            for (int64_t t = 0; t < Sk * d; ++t)
+                dkbh[t] = dvbh[t] = 0.0;
+            for (int64_t i = 0; i < Sq; ++i) {
+                const uint16_t *qi = q + (bh * Sq + i) * d;
+                const uint16_t *doi = dout + (bh * Sq + i) * d;
+                double *dqi = dq + (bh * Sq + i) * d;
+                for (int64_t t = 0; t < d; ++t)
+                    dqi[t] = 0.0;
+                const int64_t nv = visible_keys(i, Sq, Sk, causal);
+                if (nv == 0)
+                    continue;
+                /* P_i by the definition (two-pass safe softmax) */
+                score_row(qi, kbh, nv, d, sc, p);
+                double m = -INFINITY;
+                for (int64_t j = 0; j < nv; ++j)
+                    if (p[j] > m)
+                        m = p[j];
+                double l = 0.0;
+                for (int64_t j = 0; j < nv; ++j)
+                    l += exp(p[j] - m);
+                for (int64_t j = 0; j < nv; ++j)
+                    p[j] = exp(p[j] - m) / l;
+                /* dP_ij = dO_i . v_j and D_i = sum_j P_ij dP_ij */
+                double D = 0.0;
+                for (int64_t j = 0; j < nv; ++j) {
+                    const uint16_t *vj = vbh + j * d;
+                    double acc = 0.0;
+                    for (int64_t t = 0; t < d; ++t)
+                        acc += bf16_to_double(doi[t]) * bf16_to_double(vj[t]);
+                    dp[j] = acc;
+                    D += p[j] * acc;
+                }
+                for (int64_t j = 0; j < nv; ++j) {
+                    const double ds = p[j] * (dp[j] - D);
+                    const uint16_t *kj = kbh + j * d;
+                    double *dkj = dkbh + j * d, *dvj = dvbh + j * d;
+                    for (int64_t t = 0; t < d; ++t) {
+                        dqi[t] += sc * ds * bf16_to_double(kj[t]);
+                        dkj[t] += sc * ds * bf16_to_double(qi[t]);
+                        dvj[t] += p[j] * bf16_to_double(doi[t]);
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return failed ? -4 : 0;
+}

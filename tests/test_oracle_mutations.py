@@ -37,6 +37,12 @@ MUTATIONS = {
     "masked_ignores_mask": ("                if (vis[j])\n                    idx[n++] = j;",
                             "                if (vis[j] || 1)\n                    idx[n++] = j;"),
     "masked_drops_scale": ("                s[a] = sc * dot;", "                s[a] = dot;"),
+    "backward_drops_D": ("                    const double ds = p[j] * (dp[j] - D);",
+                         "                    const double ds = p[j] * dp[j];"),
+    "backward_dk_unscaled": ("                        dkj[t] += sc * ds * bf16_to_double(qi[t]);",
+                             "                        dkj[t] += ds * bf16_to_double(qi[t]);"),
+    "backward_dv_uses_ds": ("                        dvj[t] += p[j] * bf16_to_double(doi[t]);",
+                            "                        dvj[t] += ds * bf16_to_double(doi[t]);"),
     "combine_weights_unnormalised": ("            double w = exp(lse_parts[c * n_rows + r] - L);",
                                      "            double w = exp(lse_parts[c * n_rows + r] - M);"),
 }
@@ -55,6 +61,7 @@ def test_planted_mistake_is_caught(name, tmp_path):
                     "-o", str(so), "-lm"], check=True)
     env = dict(os.environ, ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_backward_pins.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutation {name} survived the oracle pins:\n{r.stdout[-2000:]}"
