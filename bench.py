@@ -10,7 +10,8 @@ of the tiled prefill kernel). Prints ONE JSON line on rank 0.
             Q, K, V and D2H of O, LSE are inside the timed region
   roofline  achieved / measured bf16 tensor peak for the prefill kernel
   verify    the decode-shaped split-KV path (B=16, H=32, Sq=5, Sk=4096) against
-            the measured HBM bandwidth
+            the measured HBM bandwidth (also as a draft tree and from paged caches)
+  backward  dQ, dK, dV on the same workload (2.5x the forward's FLOPs)
   cpu_baseline  the fp64 oracle on a bounded sample of rows, host cores
 
 --impl reference times the fp64 CPU oracle instead (the only reference arm
@@ -257,6 +258,39 @@ def run_reference(args, world, rank):
     return 0
 
 
+def measure_backward(w, device, sptr, args, peaks):
+    from exact_tiled_attention_03_gb300 import _capi
+
+    q, k, v = (t.to(device) for t in make_qkv(w))
+    g = torch.Generator(device=device).manual_seed(w.seed + 1)
+    do = torch.randn(q.shape, generator=g, device=device).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=device)
+    _capi.check(_capi.fa_forward(q, k, v, o, lse, w.B, w.H, w.Sq, w.Sk, w.d, w.causal, w.scale,
+                                 sptr), "fa_forward")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nb = _capi.fa_backward_workspace_size(w.B, w.H, w.Sq, w.Sk, w.d)
+    ws = torch.empty(nb, dtype=torch.uint8, device=device)
+
+    def step():
+        st = _capi.fa_backward(q, k, v, o, lse, do, dq, dk, dv, w.B, w.H, w.Sq, w.Sk, w.d,
+                               w.causal, w.scale, ws, nb, sptr)
+        if st != 0:
+            raise _capi.FAError(st, "fa_backward")
+
+    for _ in range(args.warmup):
+        step()
+    n = max(10, args.steps // 4)
+    per = time_steps(step, n, torch.cuda.current_stream(device)) / n
+    _capi.check(_capi.fa_device_status(sptr), "device status after backward")
+    flops = 2.5 * w.exact_flops()
+    tf = flops / per / 1e12
+    return {"workload": w.name, "ms_per_step": per * 1e3, "TFLOP/s": tf,
+            "frac_bf16_peak": tf / peaks["bf16_tflops"], "flops_per_step": flops,
+            "launches_per_step": 3, "kernels": "prep + dK/dV (4 GEMMs) + dQ (3 GEMMs)"}
+
+
+
 def measure_verify_variants(wv, device, sptr, args, peaks):
     """GB/s of the verify workload as a draft tree (random trees over the 5
     candidates) and read from a paged cache (random block table; page sizes
@@ -426,6 +460,12 @@ def run_ours(args, world, rank, local):
                   "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, 1.0)}
         del qv, kv_, vv, ov, lv, ws
 
+    # the backward pass on the same workload (dQ, dK, dV by recomputation from
+    # LSE); algorithmic FLOPs: 5 GEMMs of 2*d per visible pair = 2.5x forward
+    backward = None
+    if not args.no_backward:
+        backward = measure_backward(w, device, sptr, args, peaks)
+
     # the verify step's tree-mask and paged-cache forms, same bytes and roofline
     verify_ext = None
     if not args.no_verify:
@@ -456,7 +496,8 @@ def run_ours(args, world, rank, local):
                          "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, 1.0)},
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
-            "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "cpu_baseline": cpu,
+            "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "backward": backward,
+            "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": args.steps,  # one prefill kernel per timed step
             "gpu": torch.cuda.get_device_name(device),
@@ -478,6 +519,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -38,6 +38,8 @@ SIGNATURES = {
     "fa_verify_auto_splits": (_I32, [_I64] * 5),
     "fa_verify_forward_static": (_I32, _ATTN + [_I32, _P]),
     "fa_forward_host": (_I32, _ATTN + [_P, _SZ, _P]),
+    "fa_backward": (_I32, [_P] * 9 + [_I64] * 5 + [_I32, _F32, _P, _SZ, _P]),
+    "fa_backward_workspace_size": (_SZ, [_I64] * 5),
     "fa_verify_tree_forward": (_I32, [_P] * 5 + [_I64] * 5 + [_P, _F32, _I32, _P, _SZ, _P]),
     "fa_verify_paged_forward": (_I32, [_P] * 7 + [_I64] * 8 + [_I32, _P, _F32, _I32, _P, _SZ, _P]),
     "fa_forward_host_workspace_size": (_SZ, [_I64] * 5),
@@ -154,6 +156,17 @@ def fa_verify_paged_forward(q, k_pages, v_pages, block_table, seq_lens, o, lse, 
         _ptr(lse), B, H, Sq, d, num_pages, page_size, max_pages_per_seq, max_seq_len,
         int(bool(causal)), _ptr(tree_mask), float(scale), int(n_split), _ptr(workspace),
         int(ws_bytes), _stream(stream))
+
+
+def fa_backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, Sq, Sk, d, causal, scale, workspace=None,
+                ws_bytes=0, stream=None) -> int:
+    return load().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, H, Sq, Sk, d, int(bool(causal)),
+                              float(scale), _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def fa_backward_workspace_size(B, H, Sq, Sk, d) -> int:
+    return load().fa_backward_workspace_size(B, H, Sq, Sk, d)
 
 
 def fa_forward_host(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, workspace=None, ws_bytes=0,

@@ -409,6 +409,55 @@ fa_status_t fa_verify_paged_forward(const void *q, const void *k_pages, const vo
                          ns, workspace, ws_bytes, opt);
 }
 
+size_t fa_backward_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d)
+{
+    if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || d <= 0)
+        return 0;
+    return backward_workspace_bytes(B * H, Sq);
+}
+
+fa_status_t fa_backward(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                        int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                        float scale, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!dout || !dq || !dk || !dv)
+        return FA_ERR_INVALID_ARG;
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    const size_t need = backward_workspace_bytes(B * H, Sq);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool owned = false;
+    if (workspace) {
+        if (ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return FA_ERR_WORKSPACE;
+    } else {
+        if (cudaMallocAsync(&workspace, need, s) != cudaSuccess)
+            return FA_ERR_CUDA;
+        owned = true;
+    }
+    BackwardProblem bp;
+    bp.fwd = make_problem(q, k, v, nullptr, nullptr, B, H, Sq, Sk, d, causal, scale, stream,
+                          di->status);
+    bp.o = o;
+    bp.lse = lse;
+    bp.dout = dout;
+    bp.dq = dq;
+    bp.dk = dk;
+    bp.dv = dv;
+    bp.workspace = workspace;
+    st = launch_backward_sm103(bp);
+    if (owned && cudaFreeAsync(workspace, s) != cudaSuccess && st == FA_OK)
+        st = FA_ERR_CUDA;
+    return st;
+}
+
 size_t fa_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d)
 {
     if (Sq > FA_VERIFY_MAX_SQ)

@@ -43,6 +43,19 @@ struct VerifyOptions {
     int64_t page_size = 0, num_pages = 0, max_pages = 0;
 };
 
+// The backward pass: the forward's problem plus its O, LSE, the upstream
+// gradient and the outputs.
+struct BackwardProblem {
+    Problem fwd;  // q, k, v, sizes, causal, scale, stream, status (o/lse unused)
+    const void *o;
+    const float *lse;
+    const void *dout;
+    void *dq, *dk, *dv;
+    void *workspace;  // backward_workspace_bytes(B*H, Sq) bytes
+};
+size_t backward_workspace_bytes(int64_t BH, int64_t Sq);
+fa_status_t launch_backward_sm103(const BackwardProblem &bp);
+
 // Launchers. Each validates nothing (fa_abi.cu does) and returns FA_OK or
 // FA_ERR_CUDA.
 fa_status_t launch_prefill_sm103(const Problem &p);

@@ -193,6 +193,31 @@ fa_status_t fa_verify_paged_forward(const void *q, const void *k_pages, const vo
                                     void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Backward pass of the attention forward (prefill path): given the forward's
+ * inputs, its outputs O and LSE, and the upstream gradient dO, writes dQ, dK,
+ * dV. P is never stored: its tiles are recomputed from Q, K and LSE
+ * ("Warmup Guide — Inference Optimization at Depth", Chapter 4), i.e.
+ *     P = exp(scale * Q K^T - LSE) (masked),  D_i = dO_i . O_i,
+ *     dV = P^T dO,  dS = P o (dO V^T - D),  dK = scale * dS^T Q,
+ *     dQ = scale * dS K.
+ *   q, k, v, o, lse, causal, scale : as passed to / returned by fa_forward.
+ *   dout      : device bf16 [B, H, Sq, d].
+ *   dq        : device bf16 [B, H, Sq, d];  dk, dv: device bf16 [B, H, Sk, d].
+ *   workspace : fa_backward_workspace_size() bytes of device memory (D and
+ *               LSE per padded query row), 256-byte aligned; NULL takes it
+ *               from the stream-ordered allocator on `stream`.
+ * Rows with no visible key contribute nothing. Same shape limits and errors
+ * as fa_prefill_forward.
+ */
+fa_status_t fa_backward(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                        int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                        float scale, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes fa_backward needs (0 for invalid sizes). */
+size_t fa_backward_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d);
+
+/*
  * Attention forward on HOST-resident tensors, with the transfers inside the
  * call: the end-to-end form of fa_forward for a caller whose Q, K, V live in
  * host memory and who wants O and LSE back in host memory.

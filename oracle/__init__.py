@@ -44,12 +44,16 @@ def lib():
         L.oracle_combine.argtypes = [i64, i64, i64, dblp, dblp, dblp, dblp]
         L.oracle_attention_backward.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64,
                                                 i32, f32, dblp, dblp, dblp, i32]
+        L.oracle_attention_backward_rows.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64,
+                                                     i64, i32, f32, i64, i64p, i64, i64p, i64,
+                                                     dblp, dblp, dblp, i32]
         L.oracle_attention_masked.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64,
                                               ctypes.POINTER(ctypes.c_uint8), f32, dblp, dblp, i32]
         L.oracle_max_threads.argtypes = []
         for f in (L.oracle_attention_rows, L.oracle_attention, L.oracle_probs_row,
                   L.oracle_online_rows, L.oracle_split_rows, L.oracle_max_threads,
-                  L.oracle_combine, L.oracle_attention_masked, L.oracle_attention_backward):
+                  L.oracle_combine, L.oracle_attention_masked, L.oracle_attention_backward,
+                  L.oracle_attention_backward_rows):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -211,5 +215,24 @@ def attention_backward(q, k, v, dout, causal: bool, scale: float, threads: int =
     return dq, dk, dv
 
 
-__all__ = ["attention", "attention_backward", "attention_masked", "probs_row", "online", "split", "combine",
+def attention_backward_rows(q, k, v, dout, causal: bool, scale: float, b: int, h: int, qrows,
+                            krows, threads: int = 0):
+    """dQ of the chosen query rows and dK, dV of the chosen key rows of head (b, h)."""
+    B, H, Sq, Sk, d = _dims(q, k, v)
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int64))
+    kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int64))
+    dq = np.empty((len(qr), d), dtype=np.float64)
+    dk = np.empty((len(kr), d), dtype=np.float64)
+    dv = np.empty((len(kr), d), dtype=np.float64)
+    _check(lib().oracle_attention_backward_rows(
+        _ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
+        _ptr(db, ctypes.c_uint16), B, H, Sq, Sk, d, int(bool(causal)), ctypes.c_float(scale),
+        b * H + h, _ptr(qr, ctypes.c_int64), len(qr), _ptr(kr, ctypes.c_int64), len(kr),
+        _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+        int(threads)), "attention_backward_rows")
+    return dq, dk, dv
+
+
+__all__ = ["attention", "attention_backward", "attention_backward_rows", "attention_masked", "probs_row", "online", "split", "combine",
            "max_threads", "lib"]

@@ -694,3 +694,116 @@ int oracle_attention_backward(const uint16_t *q, const uint16_t *k, const uint16
     }
     return failed ? -4 : 0;
 }
+
+/*
+ * The same gradients for chosen rows of one (b, h): dQ of the query rows in
+ * qrows, and dK, dV of the key rows in krows. Every query row's softmax row
+ * and D_i are recomputed from the definition (parallel over query rows), so
+ * this reaches long sequences where the full backward above would be slow.
+ * bh selects the head; dq_rows [nq, d], dk_rows and dv_rows [nk, d].
+ */
+int oracle_attention_backward_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                   const uint16_t *dout, int64_t B, int64_t H, int64_t Sq,
+                                   int64_t Sk, int64_t d, int causal, float scale, int64_t bh,
+                                   const int64_t *qrows, int64_t nq, const int64_t *krows,
+                                   int64_t nk, double *dq_rows, double *dk_rows, double *dv_rows,
+                                   int nthreads)
+{
+    int rc = check_args(q, k, v, B, H, Sq, Sk, d);
+    if (rc)
+        return rc;
+    if (!dout || bh < 0 || bh >= B * H || nq < 0 || nk < 0 || (nq && (!qrows || !dq_rows)) ||
+        (nk && (!krows || !dk_rows || !dv_rows)))
+        return -1;
+    for (int64_t a = 0; a < nq; ++a)
+        if (qrows[a] < 0 || qrows[a] >= Sq)
+            return -3;
+    for (int64_t a = 0; a < nk; ++a)
+        if (krows[a] < 0 || krows[a] >= Sk)
+            return -3;
+    set_threads(nthreads);
+    const double sc = (double)scale;
+    const uint16_t *kbh = k + bh * Sk * d, *vbh = v + bh * Sk * d;
+    for (int64_t t = 0; t < nk * d; ++t)
+        dk_rows[t] = dv_rows[t] = 0.0;
+    /* which query rows want dQ: position in qrows, or -1 */
+    int64_t *qslot = (int64_t *)malloc(sizeof(int64_t) * (size_t)Sq);
+    if (!qslot)
+        return -4;
+    for (int64_t i = 0; i < Sq; ++i)
+        qslot[i] = -1;
+    for (int64_t a = 0; a < nq; ++a)
+        qslot[qrows[a]] = a;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)Sk);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)Sk);
+        double *pk = (double *)calloc((size_t)(2 * nk * d + 1), sizeof(double));
+        if (!p || !dp || !pk) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < Sq; ++i) {
+            if (!p || !dp || !pk)
+                continue;
+            const int64_t nv = visible_keys(i, Sq, Sk, causal);
+            const uint16_t *qi = q + (bh * Sq + i) * d, *doi = dout + (bh * Sq + i) * d;
+            if (nv == 0)
+                continue;
+            score_row(qi, kbh, nv, d, sc, p);
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nv; ++j)
+                if (p[j] > m)
+                    m = p[j];
+            double l = 0.0;
+            for (int64_t j = 0; j < nv; ++j)
+                l += exp(p[j] - m);
+            for (int64_t j = 0; j < nv; ++j)
+                p[j] = exp(p[j] - m) / l;
+            double D = 0.0;
+            for (int64_t j = 0; j < nv; ++j) {
+                const uint16_t *vj = vbh + j * d;
+                double acc = 0.0;
+                for (int64_t t = 0; t < d; ++t)
+                    acc += bf16_to_double(doi[t]) * bf16_to_double(vj[t]);
+                dp[j] = acc;
+                D += p[j] * acc;
+            }
+            if (qslot[i] >= 0) {
+                double *dqi = dq_rows + qslot[i] * d;
+                for (int64_t t = 0; t < d; ++t)
+                    dqi[t] = 0.0;
+                for (int64_t j = 0; j < nv; ++j) {
+                    const double ds = p[j] * (dp[j] - D);
+                    const uint16_t *kj = kbh + j * d;
+                    for (int64_t t = 0; t < d; ++t)
+                        dqi[t] += sc * ds * bf16_to_double(kj[t]);
+                }
+            }
+            for (int64_t a = 0; a < nk; ++a) {
+                const int64_t j = krows[a];
+                if (j >= nv)
+                    continue;
+                const double ds = p[j] * (dp[j] - D);
+                for (int64_t t = 0; t < d; ++t) {
+                    pk[a * d + t] += sc * ds * bf16_to_double(qi[t]);
+                    pk[nk * d + a * d + t] += p[j] * bf16_to_double(doi[t]);
+                }
+            }
+        }
+        if (pk) {
+#pragma omp critical
+            for (int64_t t = 0; t < nk * d; ++t) {
+                dk_rows[t] += pk[t];
+                dv_rows[t] += pk[nk * d + t];
+            }
+        }
+        free(p);
+        free(dp);
+        free(pk);
+    }
+    free(qslot);
+    return failed ? -4 : 0;
+}

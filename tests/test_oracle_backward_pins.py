@@ -85,3 +85,16 @@ def test_single_key_routes_all_gradient_to_its_value():
     dq, dk, dv = oracle.attention_backward(q, k, v, do, False, w.scale)
     assert np.max(np.abs(dq)) == 0.0 and np.max(np.abs(dk)) == 0.0
     assert np.max(np.abs(dv[:, :, 0] - to_f64(do).sum(axis=2))) < 1e-13
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_rows_equal_the_full_backward(causal):
+    """The row-subset backward agrees with the full one (different loop order, same math)."""
+    w, q, k, v, do = case(2, 3, 70, 90, 16, causal, seed=79, factor=2.0)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal, w.scale)
+    qrows, krows = [0, 5, 69, 33], [0, 1, 89, 40, 22]
+    for b, h in ((0, 0), (1, 2)):
+        rq, rk, rv = oracle.attention_backward_rows(q, k, v, do, causal, w.scale, b, h, qrows, krows)
+        assert np.max(np.abs(rq - dq[b, h, qrows])) < TOL
+        assert np.max(np.abs(rk - dk[b, h, krows])) < TOL
+        assert np.max(np.abs(rv - dv[b, h, krows])) < TOL
