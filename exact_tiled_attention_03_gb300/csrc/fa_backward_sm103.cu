@@ -21,6 +21,14 @@
 //   * fa_bwd_dq_kernel: one CTA per 128-row query tile; for every key tile
 //     it sees: S = Q K_j^T, dP = dO V_j^T, then one thread per query rebuilds
 //     dS and dQ += dS K_j (A from TMEM).
+// Both gradient kernels split each 128-column score tile into two halves of
+// 64 columns with their own barriers: the MMA warp issues half 0's scores,
+// then half 1's; warps 0-3 rebuild half 0 while the tensor core computes
+// half 1, and half 0's gradient MMAs run while warps 4-7 rebuild half 1.
+// The two warps of a sub-partition share TMEM lanes (lane quarter = warp
+// mod 4) and split the columns. Each half packs its bf16 result into its own
+// first 32 columns (0-31 and 64-95), so neither half overwrites columns the
+// other has yet to read.
 // The warp roles, TMA ring, mbarrier waits (bounded) and descriptor
 // encodings are those of the forward kernel.
 #include <cmath>
@@ -32,9 +40,11 @@ namespace fa {
 namespace bwd {
 
 constexpr int kBlock = 128;             // keys or queries per tile = TMEM lanes
-constexpr int kThreads = 192;           // warps 0-3 math, warp 4 producer, warp 5 MMA
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kMathThreads = 256;       // warps 0-7: lane quarter warp % 4, column half warp / 4
+constexpr int kThreads = kMathThreads + 64;  // + warp 8 producer, warp 9 MMA
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kHalf = kBlock / 2;        // score columns per half
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = kBlock * 128;  // 128 rows x 64 columns bf16
 constexpr int kChunk = 32;               // TMEM columns a math thread handles at a time
@@ -103,16 +113,18 @@ __global__ void __launch_bounds__(256)
 __device__ __forceinline__ uint32_t pk2(float a, float b) { return pack_bf16x2(a, b); }
 
 // The epilogue of both gradient kernels: a 128 x D fp32 tile in TMEM (this
-// thread's lane = row r) times `mul`, to bf16, through shared memory (Q-tile
-// sized staging at `stage`, swizzled like the TMA box), then TMA-stored.
+// thread's lane = row r; `taddr` addresses column 0 of that lane) times
+// `mul`, to bf16, through shared memory (Q-tile sized staging at `stage`,
+// swizzled like the TMA box), then TMA-stored. Column half `half` of the
+// tile is this thread's; all math threads take part.
 template <int D>
 __device__ __forceinline__ void store_tile(uint32_t taddr, float mul, bool have, uint8_t *stage,
                                            const CUtensorMap *map, int row0, int bh, int r,
-                                           uint32_t bar_id)
+                                           int half, uint32_t bar_id)
 {
     const uint32_t st_a = smem_u32(stage);
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t v[32];
         if (have) {
             tmem_ld32_wait(taddr + c0, v);
@@ -133,14 +145,14 @@ __device__ __forceinline__ void store_tile(uint32_t taddr, float mul, bool have,
         }
     }
     fence_proxy_async_smem();
-    named_bar_sync(bar_id, 128);
-    if (r == 0) {
+    named_bar_sync(bar_id, kMathThreads);
+    if (r == 0 && half == 0) {
         for (int b = 0; b < D / 64; ++b)
             tma_store_3d(map, stage + b * kBoxBytes, b * 64, row0, bh);
         tma_store_commit();
         tma_store_wait_read_all();
     }
-    named_bar_sync(bar_id, 128);
+    named_bar_sync(bar_id, kMathThreads);
 }
 
 // ---------------------------------------------------------------- dK, dV
@@ -160,8 +172,8 @@ struct KvCfg {
 struct KvBars {
     uint64_t kv_full;
     uint64_t full[4], empty[4];
-    uint64_t st_full;  // S^T and dP^T of the current query tile in TMEM
-    uint64_t p_full;   // P^T and dS^T written back (4 warp arrivals)
+    uint64_t st_full[2];  // half h of S^T and dP^T of the current query tile in TMEM
+    uint64_t p_full[2];   // half h of P^T and dS^T written back (4 warp arrivals)
     uint64_t o_done;   // last dV / dK MMAs completed
     uint64_t drain;
     uint32_t tmem_base;
@@ -201,8 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        mbar_init(&bars->st_full, 1);
-        mbar_init(&bars->p_full, 4);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bars->st_full[h], 1);
+            mbar_init(&bars->p_full[h], 4);
+        }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
@@ -248,76 +262,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0 && n_q > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlock, kBlock, false, false);
+            constexpr uint32_t idesc_h = idesc_bf16_f32(kBlock, kHalf, false, false);
             constexpr uint32_t idesc_g = idesc_bf16_f32(kBlock, D, false, true);
             const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
             const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
             const uint32_t ring = smem_u32(smem + C::kOffRing);
-            bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.status);
-            for (int n = 0; n < n_q && ok; ++n) {
-                const int s = n % C::kStages;
-                ok = mbar_wait(&bars->full[s], (n / C::kStages) & 1, abort_flag, p.status);
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-                const uint32_t sq = ring + s * C::kStageBytes, sdo = sq + C::kTile;
+            // Half h of S^T = K Q^T and dP^T = V dO^T: the query rows
+            // [64h, 64h + 64) of the tile (both operands K-major).
+            auto issue_scores = [&](int n, int h) {
+                const uint32_t sq = ring + (n % C::kStages) * C::kStageBytes + h * kHalf * 128;
                 const uint64_t dq0 = smem_desc_sw128(sq, 16, 1024);
-                const uint64_t ddo0 = smem_desc_sw128(sdo, 16, 1024);
-                // S^T = K Q^T and dP^T = V dO^T (both operands K-major)
+                const uint64_t ddo0 = smem_desc_sw128(sq + C::kTile, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColS, dk0 + koff, dq0 + koff, idesc_s, kk > 0);
+                    umma_bf16_ss(tmem + C::kColS + h * kHalf, dk0 + koff, dq0 + koff, idesc_h,
+                                 kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColDP, dv0 + koff, ddo0 + koff, idesc_s, kk > 0);
+                    umma_bf16_ss(tmem + C::kColDP + h * kHalf, dv0 + koff, ddo0 + koff, idesc_h,
+                                 kk > 0);
                 }
-                umma_commit(&bars->st_full);
-                ok = mbar_wait(&bars->p_full, n & 1, abort_flag, p.status);
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-                // dV += P^T dO and dK += dS^T Q: A from TMEM, B (dO, Q) MN-major
-                const uint64_t bdo = smem_desc_sw128(sdo, kBoxBytes, 1024);
+                umma_commit(&bars->st_full[h]);
+            };
+            // dV += P^T dO and dK += dS^T Q over the query rows of half h:
+            // A (bf16 pairs) from the half's first 32 TMEM columns, B (dO, Q)
+            // MN-major from shared memory.
+            auto issue_grads = [&](int n, int h) {
+                const uint32_t sq = ring + (n % C::kStages) * C::kStageBytes;
                 const uint64_t bq = smem_desc_sw128(sq, kBoxBytes, 1024);
+                const uint64_t bdo = smem_desc_sw128(sq + C::kTile, kBoxBytes, 1024);
 #pragma unroll
-                for (int kk = 0; kk < kBlock / 16; ++kk)
-                    umma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                for (int k4 = 0; k4 < kHalf / 16; ++k4) {
+                    const int kk = h * (kHalf / 16) + k4;
+                    umma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + h * kHalf + k4 * 8,
                                  bdo + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (n > 0 || kk > 0) ? 1u : 0u);
+                }
 #pragma unroll
-                for (int kk = 0; kk < kBlock / 16; ++kk)
-                    umma_bf16_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                for (int k4 = 0; k4 < kHalf / 16; ++k4) {
+                    const int kk = h * (kHalf / 16) + k4;
+                    umma_bf16_ts(tmem + C::kColDK, tmem + C::kColDP + h * kHalf + k4 * 8,
                                  bq + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (n > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->empty[s]);
+                }
+            };
+            bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.status) &&
+                      mbar_wait(&bars->full[0], 0, abort_flag, p.status);
+            if (ok) {
+                tc_fence_after_sync();
+                issue_scores(0, 0);
+                issue_scores(0, 1);
+            }
+            // Tile n+1's half-0 scores are issued between tile n's two
+            // gradient halves, so the tensor core has work while either
+            // group of math warps is busy. MMAs from one thread run in
+            // issue order, which orders each TMEM reuse after its reader.
+            for (int n = 0; n < n_q && ok; ++n) {
+                ok = mbar_wait(&bars->p_full[0], n & 1, abort_flag, p.status);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                issue_grads(n, 0);
+                const bool next = n + 1 < n_q;
+                if (next) {
+                    ok = mbar_wait(&bars->full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1,
+                                   abort_flag, p.status);
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    issue_scores(n + 1, 0);
+                }
+                ok = mbar_wait(&bars->p_full[1], n & 1, abort_flag, p.status);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                issue_grads(n, 1);
+                umma_commit(&bars->empty[n % C::kStages]);
+                if (next)
+                    issue_scores(n + 1, 1);
             }
             umma_commit(&bars->o_done);
             umma_commit(&bars->drain);
             mbar_wait_drain(&bars->drain, 0, p.status);
         }
     } else {
-        // ------------------------------------------------------------ math warpgroup
-        const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
+        // ------------------------------------------------------------ math warps
+        const int quarter = warp & 3, half = warp >> 2;
+        const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane
         const int key = kv0 + r;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS, tDP = tmem + lane_base + C::kColDP;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::kColS + half * kHalf;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + half * kHalf;
         const float sl2 = p.scale_log2;
         bool ok = true;
         for (int n = 0; n < n_q && ok; ++n) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->st_full, n & 1, abort_flag, p.status));
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->st_full[half], n & 1, abort_flag, p.status));
             if (!ok)
                 break;
             tc_fence_after_sync();
-            const int q0 = (qt0 + n) * kBlock;
+            const int q0 = (qt0 + n) * kBlock + half * kHalf;  // first query of this half
             const float *vec = reinterpret_cast<const float *>(smem + C::kOffVec +
-                                                               (n % C::kStages) * 1024);
+                                                               (n % C::kStages) * 1024) +
+                               half * kHalf;
             // mask: key beyond Sk, or (causal) key after the query's last visible key
             const bool tile_masked = key >= p.Sk || (p.causal && kv0 + kBlock - 1 > q0 + off);
 #pragma unroll
-            for (int c0 = 0; c0 < kBlock; c0 += kChunk) {
+            for (int c0 = 0; c0 < kHalf; c0 += kChunk) {
                 uint32_t sr[kChunk], dr[kChunk];
                 tmem_ld32_wait(tS + c0, sr);
                 tmem_ld32_wait(tDP + c0, dr);
@@ -338,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pp[c / 2] = pk2(pv[0], pv[1]);
                     pd[c / 2] = pk2(dv[0], dv[1]);
                 }
-                // P^T and dS^T (bf16 pairs) over their own, already read columns
+                // P^T and dS^T (bf16 pairs) over this half's own, already read columns
                 tmem_st16(tS + c0 / 2, pp);
                 tmem_st16(tDP + c0 / 2, pd);
             }
@@ -346,19 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bars->p_full);
+                mbar_arrive(&bars->p_full[half]);
         }
         // ------------------------------------------------------------ epilogue
         if (ok && n_q > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort_flag, p.status));
             tc_fence_after_sync();
         }
-        if (ok && !*reinterpret_cast<volatile int *>(abort_flag)) {
+        // All math threads take the epilogue (and its barriers) or none does.
+        const bool skip =
+            named_bar_or(1, kMathThreads, !ok || *reinterpret_cast<volatile int *>(abort_flag));
+        if (!skip) {
             uint8_t *stage = smem + C::kOffRing;  // the ring is idle now
             store_tile<D>(tmem + lane_base + C::kColDV, 1.0f, n_q > 0, stage, &tm_dv, kv0, bh, r,
-                          1);
+                          half, 2);
             store_tile<D>(tmem + lane_base + C::kColDK, p.scale, n_q > 0, stage, &tm_dk, kv0, bh,
-                          r, 1);
+                          r, half, 2);
         }
     }
     tc_fence_before_sync();
@@ -383,7 +440,8 @@ struct QCfg {
 struct QBars {
     uint64_t q_full;
     uint64_t full[4], empty[4];
-    uint64_t st_full, p_full, o_done, drain;
+    uint64_t st_full[2], p_full[2];  // per column half, as in KvBars
+    uint64_t o_done, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -415,8 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        mbar_init(&bars->st_full, 1);
-        mbar_init(&bars->p_full, 4);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bars->st_full[h], 1);
+            mbar_init(&bars->p_full[h], 4);
+        }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
@@ -459,69 +519,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0 && n_kv > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlock, kBlock, false, false);
+            constexpr uint32_t idesc_h = idesc_bf16_f32(kBlock, kHalf, false, false);
             constexpr uint32_t idesc_g = idesc_bf16_f32(kBlock, D, false, true);
             const uint64_t aq0 = smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
             const uint64_t ado0 = smem_desc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
             const uint32_t ring = smem_u32(smem + C::kOffRing);
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int s = j % C::kStages;
-                ok = mbar_wait(&bars->full[s], (j / C::kStages) & 1, abort_flag, p.status);
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-                const uint32_t sk = ring + s * C::kStageBytes, sv = sk + C::kTile;
+            // Half h of S = Q K^T and dP = dO V^T: the keys [64h, 64h + 64)
+            // of the tile (both operands K-major).
+            auto issue_scores = [&](int j, int h) {
+                const uint32_t sk = ring + (j % C::kStages) * C::kStageBytes + h * kHalf * 128;
                 const uint64_t bk0 = smem_desc_sw128(sk, 16, 1024);
-                const uint64_t bv0 = smem_desc_sw128(sv, 16, 1024);
-                // S = Q K^T and dP = dO V^T (both operands K-major)
+                const uint64_t bv0 = smem_desc_sw128(sk + C::kTile, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColS, aq0 + koff, bk0 + koff, idesc_s, kk > 0);
+                    umma_bf16_ss(tmem + C::kColS + h * kHalf, aq0 + koff, bk0 + koff, idesc_h,
+                                 kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColDP, ado0 + koff, bv0 + koff, idesc_s, kk > 0);
+                    umma_bf16_ss(tmem + C::kColDP + h * kHalf, ado0 + koff, bv0 + koff, idesc_h,
+                                 kk > 0);
                 }
-                umma_commit(&bars->st_full);
-                ok = mbar_wait(&bars->p_full, j & 1, abort_flag, p.status);
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-                // dQ += dS K: A = dS from TMEM, B = K MN-major
+                umma_commit(&bars->st_full[h]);
+            };
+            // dQ += dS K over the keys of half h: A = dS (bf16 pairs) from
+            // the half's first 32 TMEM columns, B = K MN-major.
+            auto issue_grad = [&](int j, int h) {
+                const uint32_t sk = ring + (j % C::kStages) * C::kStageBytes;
                 const uint64_t bkm = smem_desc_sw128(sk, kBoxBytes, 1024);
 #pragma unroll
-                for (int kk = 0; kk < kBlock / 16; ++kk)
-                    umma_bf16_ts(tmem + C::kColDQ, tmem + C::kColS + kk * 8,
+                for (int k4 = 0; k4 < kHalf / 16; ++k4) {
+                    const int kk = h * (kHalf / 16) + k4;
+                    umma_bf16_ts(tmem + C::kColDQ, tmem + C::kColS + h * kHalf + k4 * 8,
                                  bkm + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->empty[s]);
+                }
+            };
+            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status) &&
+                      mbar_wait(&bars->full[0], 0, abort_flag, p.status);
+            if (ok) {
+                tc_fence_after_sync();
+                issue_scores(0, 0);
+                issue_scores(0, 1);
+            }
+            // The same interleaving as the dK/dV kernel.
+            for (int j = 0; j < n_kv && ok; ++j) {
+                ok = mbar_wait(&bars->p_full[0], j & 1, abort_flag, p.status);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                issue_grad(j, 0);
+                const bool next = j + 1 < n_kv;
+                if (next) {
+                    ok = mbar_wait(&bars->full[(j + 1) % C::kStages], ((j + 1) / C::kStages) & 1,
+                                   abort_flag, p.status);
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    issue_scores(j + 1, 0);
+                }
+                ok = mbar_wait(&bars->p_full[1], j & 1, abort_flag, p.status);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                issue_grad(j, 1);
+                umma_commit(&bars->empty[j % C::kStages]);
+                if (next)
+                    issue_scores(j + 1, 1);
             }
             umma_commit(&bars->o_done);
             umma_commit(&bars->drain);
             mbar_wait_drain(&bars->drain, 0, p.status);
         }
     } else {
-        const int r = warp * 32 + lane;  // query row within the tile = TMEM lane
+        const int quarter = warp & 3, half = warp >> 2;
+        const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
         const int i = q0 + r;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS, tDP = tmem + lane_base + C::kColDP;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::kColS + half * kHalf;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + half * kHalf;
         const float sl2 = p.scale_log2;
         const size_t vrow = static_cast<size_t>(bh) * p.Sq_pad + i;
         const float l2 = p.lse2[vrow], Di = p.Dvec[vrow];  // padded rows: +inf, 0
         const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
         bool ok = true;
         for (int j = 0; j < n_kv && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->st_full, j & 1, abort_flag, p.status));
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->st_full[half], j & 1, abort_flag, p.status));
             if (!ok)
                 break;
             tc_fence_after_sync();
             const bool tile_masked = j >= mask_from;
-            const int key0 = j * kBlock;
+            const int key0 = j * kBlock + half * kHalf;  // first key of this half
 #pragma unroll
-            for (int c0 = 0; c0 < kBlock; c0 += kChunk) {
+            for (int c0 = 0; c0 < kHalf; c0 += kChunk) {
                 uint32_t sr[kChunk], dr[kChunk];
                 tmem_ld32_wait(tS + c0, sr);
                 tmem_ld32_wait(tDP + c0, dr);
@@ -538,21 +631,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     pd[c / 2] = pk2(ds[0], ds[1]);
                 }
-                tmem_st16(tS + c0 / 2, pd);  // dS (bf16 pairs) over S's read columns
+                tmem_st16(tS + c0 / 2, pd);  // dS (bf16 pairs) over this half's read columns
             }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bars->p_full);
+                mbar_arrive(&bars->p_full[half]);
         }
         if (ok && n_kv > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort_flag, p.status));
             tc_fence_after_sync();
         }
-        if (ok && !*reinterpret_cast<volatile int *>(abort_flag))
+        const bool skip =
+            named_bar_or(1, kMathThreads, !ok || *reinterpret_cast<volatile int *>(abort_flag));
+        if (!skip)
             store_tile<D>(tmem + lane_base + C::kColDQ, p.scale, n_kv > 0, smem + C::kOffQ,
-                          &tm_dq, q0, bh, r, 1);
+                          &tm_dq, q0, bh, r, half, 2);
     }
     tc_fence_before_sync();
     __syncthreads();
