@@ -134,6 +134,30 @@ def make_qkv(w: Workload, device="cpu"):
     return q, k, v
 
 
+def make_qkv_fp8(w: Workload, device="cpu"):
+    """E4M3 inputs for workload ``w``: the same N(0, 1) draws as ``make_qkv``
+    (seed, order, q_factor), each tensor divided by a power-of-two descale
+    2^ceil(log2(amax / 448)) so that it fits E4M3's range without clamping, then
+    cast by torch (round to nearest even). Returns (q8, k8, v8, descales), with
+    q8/k8/v8 torch.float8_e4m3fn [B, H, S, d] and descales = (dq, dk, dv) floats:
+    an input byte stands for descale * its E4M3 value."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn(w.q_shape, generator=g, dtype=torch.float32)
+    if w.q_factor != 1.0:
+        q.mul_(w.q_factor)
+    k = torch.randn(w.kv_shape, generator=g, dtype=torch.float32)
+    v = torch.randn(w.kv_shape, generator=g, dtype=torch.float32)
+    out, descales = [], []
+    for t in (q, k, v):
+        amax = float(t.abs().max()) if t.numel() else 1.0
+        ds = 2.0 ** math.ceil(math.log2(max(amax, 1e-30) / 448.0))
+        out.append((t / ds).to(torch.float8_e4m3fn))
+        descales.append(ds)
+    if device != "cpu":
+        out = [t.to(device) for t in out]
+    return out[0], out[1], out[2], tuple(descales)
+
+
 def sample_rows(w: Workload, per_head: int | None = None, n_total: int | None = None,
                 seed: int = 12345, tile: int = 128):
     """Seeded (b, h, i) query rows for sampled parity checks at full size.

@@ -50,10 +50,17 @@ def lib():
         L.oracle_attention_masked.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64,
                                               ctypes.POINTER(ctypes.c_uint8), f32, dblp, dblp, i32]
         L.oracle_max_threads.argtypes = []
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        fp8 = [u8p, u8p, u8p, i64, i64, i64, i64, i64, i32, f32, f32, f32, f32, i32]
+        L.oracle_attention_fp8_rows.argtypes = fp8 + [i64p, i64, dblp, dblp, i32]
+        L.oracle_attention_fp8.argtypes = fp8 + [dblp, dblp, i32]
+        L.oracle_e4m3_decode.argtypes = [u8p, i64, dblp]
+        L.oracle_e4m3_round.argtypes = [dblp, i64, dblp]
         for f in (L.oracle_attention_rows, L.oracle_attention, L.oracle_probs_row,
                   L.oracle_online_rows, L.oracle_split_rows, L.oracle_max_threads,
                   L.oracle_combine, L.oracle_attention_masked, L.oracle_attention_backward,
-                  L.oracle_attention_backward_rows):
+                  L.oracle_attention_backward_rows, L.oracle_attention_fp8_rows,
+                  L.oracle_attention_fp8, L.oracle_e4m3_decode, L.oracle_e4m3_round):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -234,5 +241,64 @@ def attention_backward_rows(q, k, v, dout, causal: bool, scale: float, b: int, h
     return dq, dk, dv
 
 
-__all__ = ["attention", "attention_backward", "attention_backward_rows", "attention_masked", "probs_row", "online", "split", "combine",
-           "max_threads", "lib"]
+def _bytes(t: torch.Tensor) -> np.ndarray:
+    """E4M3 tensor (torch.float8_e4m3fn) or uint8 bytes -> contiguous uint8 array."""
+    if t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"FP8 oracle inputs are E4M3 bytes, got {t.dtype}")
+    return t.detach().to("cpu").contiguous().numpy()
+
+
+def e4m3_decode(x) -> np.ndarray:
+    """Exact value of each E4M3 byte (NaN for the NaN codes), fp64."""
+    b = np.ascontiguousarray(np.asarray(x, dtype=np.uint8)).reshape(-1)
+    out = np.empty(b.shape, dtype=np.float64)
+    _check(lib().oracle_e4m3_decode(_ptr(b, ctypes.c_uint8), b.size, _ptr(out, ctypes.c_double)),
+           "e4m3_decode")
+    return out
+
+
+def e4m3_round(y) -> np.ndarray:
+    """Nearest E4M3 value (ties to even, |y| > 448 clamped), fp64."""
+    a = np.ascontiguousarray(np.asarray(y, dtype=np.float64)).reshape(-1)
+    out = np.empty(a.shape, dtype=np.float64)
+    _check(lib().oracle_e4m3_round(_ptr(a, ctypes.c_double), a.size, _ptr(out, ctypes.c_double)),
+           "e4m3_round")
+    return out
+
+
+def attention_fp8(q8, k8, v8, causal: bool, scale: float, descale=(1.0, 1.0, 1.0),
+                  quantize_p: bool = True, rows=None, threads: int = 0):
+    """FP8 forward: E4M3 inputs times per-tensor descales, P rounded to E4M3 when
+    ``quantize_p`` (else the definition on the decoded inputs). Shapes and return
+    values as ``attention``."""
+    if q8.dim() != 4 or k8.shape != v8.shape or k8.dim() != 4:
+        raise ValueError("expected q [B,H,Sq,d] and k, v [B,H,Sk,d]")
+    B, H, Sq, d = q8.shape
+    Sk = k8.shape[2]
+    qb, kb, vb = _bytes(q8), _bytes(k8), _bytes(v8)
+    L = lib()
+    args = (_ptr(qb, ctypes.c_uint8), _ptr(kb, ctypes.c_uint8), _ptr(vb, ctypes.c_uint8),
+            B, H, Sq, Sk, d, int(bool(causal)), ctypes.c_float(scale),
+            ctypes.c_float(descale[0]), ctypes.c_float(descale[1]), ctypes.c_float(descale[2]),
+            int(bool(quantize_p)))
+    if rows is None:
+        o = np.empty((B, H, Sq, d), dtype=np.float64)
+        lse = np.empty((B, H, Sq), dtype=np.float64)
+        _check(L.oracle_attention_fp8(*args, _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                      int(threads)), "attention_fp8")
+        return o, lse
+    r = _rows_array(rows, B, H, Sq)
+    n = r.shape[0]
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _check(L.oracle_attention_fp8_rows(*args, _ptr(r, ctypes.c_int64), n,
+                                       _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                       int(threads)), "attention_fp8_rows")
+    return o, lse
+
+
+__all__ = ["attention", "attention_backward", "attention_backward_rows", "attention_masked",
+           "attention_fp8", "e4m3_decode", "e4m3_round", "probs_row", "online", "split",
+           "combine", "max_threads", "lib"]

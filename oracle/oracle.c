@@ -807,3 +807,205 @@ int oracle_attention_backward_rows(const uint16_t *q, const uint16_t *k, const u
     free(qslot);
     return failed ? -4 : 0;
 }
+
+/* ---------------------------------------------------------------- FP8 forward
+ *
+ * "FlashAttention, speculative decoding, quantisation and parallelism", The
+ * problem it solves (FlashAttention-3 targets Hopper's asynchrony and FP8),
+ * and "Lecture 06", section 5 (FlashAttention-3: FP8 support, FP8 up to about
+ * 1.2 PFLOP/s): the same forward with Q, K and V stored as 8-bit floats. The
+ * pages name FP8 and nothing else about it; the readings taken here:
+ *   - the format is E4M3 without infinities ("e4m3fn"): 1 sign bit, 4
+ *     exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+ *     subnormals m/8 * 2^-6; S.1111.111 is NaN; the largest finite value is
+ *     1.75 * 2^8 = 448;
+ *   - one fp32 descale per tensor: the value an input byte stands for is
+ *     descale * decode(byte);
+ *   - the second product runs in FP8 as well, so P is rounded to E4M3 before
+ *     it multiplies V. The rounding is taken against a power of two at the
+ *     row's max: with x_j = s_j * log2(e) and M = ceil(max_j x_j), the weight
+ *     used is P_j = 2^-7 * e4m3(2^7 * 2^(x_j - M)) (round to nearest, ties to
+ *     even). M is an integer, so rounding against any other integer
+ *     reference gives the same P_j up to an exact power of two (outside the
+ *     subnormal range): a streaming kernel that settles its reference late
+ *     reaches the same weights;
+ *   - the row sum l = sum_j 2^(x_j - M) is taken before the rounding, so the
+ *     LSE is the definition's;
+ *   - o = sum_j P_j v_j / l and lse = ln 2 * (M + log2 l).
+ * With quantize_p = 0 the weights are not rounded and the result is the
+ * definition of attention on the decoded inputs.
+ */
+
+/* ln 2 (strict C11 has no M_LN2). */
+static const double kLn2 = 0.693147180559945309417232121458176568;
+
+/* Exact E4M3 -> double from the bit fields. */
+static double e4m3_to_double(uint8_t x)
+{
+    const int e = (x >> 3) & 15, m = x & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);        /* m/8 * 2^-6 */
+    else
+        mag = ldexp(8.0 + m, e - 10);      /* (1 + m/8) * 2^(e-7) */
+    return (x & 0x80) ? -mag : mag;
+}
+
+/*
+ * Round a finite double to the nearest E4M3 value, ties to the even mantissa,
+ * magnitudes above 448 clamped to 448. The spacing in the binade [2^e, 2^e+1)
+ * is 2^(e-3) (three mantissa bits); below 2^-6 it is the subnormal 2^-9.
+ */
+static double e4m3_round(double y)
+{
+    const double a = fabs(y);
+    if (a == 0.0 || a != a)
+        return y;
+    int k;
+    frexp(a, &k);                  /* a = f 2^k with f in [0.5, 1): floor(log2 a) = k - 1 */
+    int e = k - 1;
+    if (e < -6)
+        e = -6;
+    const double q = ldexp(1.0, e - 3);
+    const double r = a / q;        /* exact: q is a power of two */
+    double n = floor(r);
+    const double frac = r - n;
+    if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) == 1.0))
+        n += 1.0;
+    double out = n * q;
+    if (out > 448.0)
+        out = 448.0;
+    return y < 0 ? -out : out;
+}
+
+/* Decode n bytes (for the pins). */
+int oracle_e4m3_decode(const uint8_t *x, int64_t n, double *out)
+{
+    if (n < 0 || (n > 0 && (!x || !out)))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_to_double(x[i]);
+    return 0;
+}
+
+/* Round n doubles to E4M3 values (for the pins). */
+int oracle_e4m3_round(const double *y, int64_t n, double *out)
+{
+    if (n < 0 || (n > 0 && (!y || !out)))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_round(y[i]);
+    return 0;
+}
+
+/* One FP8 row over keys [0, n): the steps listed above. x: n doubles of scratch. */
+static void fp8_row(const uint8_t *qi, const uint8_t *kbh, const uint8_t *vbh, int64_t n, int64_t d,
+                    double scale, double dq, double dk, double dv, int quantize_p, double *x,
+                    double *o, double *lse)
+{
+    for (int64_t t = 0; t < d; ++t)
+        o[t] = 0.0;
+    if (n <= 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    /* s_j = scale * (dq q_i) . (dk k_j); x_j = s_j log2(e) */
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        const uint8_t *kj = kbh + j * d;
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t)
+            dot += (dq * e4m3_to_double(qi[t])) * (dk * e4m3_to_double(kj[t]));
+        x[j] = scale * dot / kLn2;
+        if (x[j] > mx)
+            mx = x[j];
+    }
+    const double M = quantize_p ? ceil(mx) : mx;
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j)
+        l += exp2(x[j] - M);
+    for (int64_t j = 0; j < n; ++j) {
+        double p = exp2(x[j] - M);
+        if (quantize_p)
+            p = ldexp(e4m3_round(ldexp(p, 7)), -7);
+        const uint8_t *vj = vbh + j * d;
+        for (int64_t t = 0; t < d; ++t)
+            o[t] += p * (dv * e4m3_to_double(vj[t]));
+    }
+    for (int64_t t = 0; t < d; ++t)
+        o[t] /= l;
+    *lse = kLn2 * (M + log2(l));
+}
+
+/*
+ * FP8 forward for a list of rows. q: E4M3 bytes [B,H,Sq,d]; k, v: [B,H,Sk,d];
+ * rows: n triples (b,h,i); o: n*d doubles; lse: n doubles.
+ */
+int oracle_attention_fp8_rows(const uint8_t *q, const uint8_t *k, const uint8_t *v, int64_t B,
+                              int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal, float scale,
+                              float q_descale, float k_descale, float v_descale, int quantize_p,
+                              const int64_t *rows, int64_t n, double *o, double *lse, int nthreads)
+{
+    int rc = check_args(q, k, v, B, H, Sq, Sk, d);
+    if (rc)
+        return rc;
+    if (n < 0 || (n > 0 && (!rows || !o || !lse)))
+        return -1;
+    for (int64_t r = 0; r < n; ++r)
+        if (!row_in_range(rows + 3 * r, B, H, Sq))
+            return -3;
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)Sk);
+        if (!x) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n; ++r) {
+            if (!x)
+                continue;
+            int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+            const uint8_t *qi = q + ((b * H + h) * Sq + i) * d;
+            const uint8_t *kbh = k + (b * H + h) * Sk * d;
+            const uint8_t *vbh = v + (b * H + h) * Sk * d;
+            fp8_row(qi, kbh, vbh, visible_keys(i, Sq, Sk, causal), d, (double)scale,
+                    (double)q_descale, (double)k_descale, (double)v_descale, quantize_p, x,
+                    o + r * d, lse + r);
+        }
+        free(x);
+    }
+    return failed ? -4 : 0;
+}
+
+/* Every row: o [B,H,Sq,d], lse [B,H,Sq] (doubles). */
+int oracle_attention_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v, int64_t B, int64_t H,
+                         int64_t Sq, int64_t Sk, int64_t d, int causal, float scale,
+                         float q_descale, float k_descale, float v_descale, int quantize_p,
+                         double *o, double *lse, int nthreads)
+{
+    int rc = check_args(q, k, v, B, H, Sq, Sk, d);
+    if (rc)
+        return rc;
+    if (!o || !lse)
+        return -1;
+    int64_t n = B * H * Sq;
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * 3 * (size_t)n);
+    if (!rows)
+        return -4;
+    for (int64_t b = 0, r = 0; b < B; ++b)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t i = 0; i < Sq; ++i, ++r) {
+                rows[3 * r] = b;
+                rows[3 * r + 1] = h;
+                rows[3 * r + 2] = i;
+            }
+    rc = oracle_attention_fp8_rows(q, k, v, B, H, Sq, Sk, d, causal, scale, q_descale, k_descale,
+                                   v_descale, quantize_p, rows, n, o, lse, nthreads);
+    free(rows);
+    return rc;
+}

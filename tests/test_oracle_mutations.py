@@ -45,6 +45,20 @@ MUTATIONS = {
                             "                        dvj[t] += ds * bf16_to_double(doi[t]);"),
     "combine_weights_unnormalised": ("            double w = exp(lse_parts[c * n_rows + r] - L);",
                                      "            double w = exp(lse_parts[c * n_rows + r] - M);"),
+    "e4m3_bias_8": ("mag = ldexp(8.0 + m, e - 10);", "mag = ldexp(8.0 + m, e - 11);"),
+    "e4m3_subnormal_step": ("mag = ldexp((double)m, -9);", "mag = ldexp((double)m, -10);"),
+    "e4m3_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) == 1.0))",
+                       "if (frac >= 0.5)"),
+    "e4m3_truncates": ("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) == 1.0))", "if (0)"),
+    "fp8_drops_q_descale": ("dot += (dq * e4m3_to_double(qi[t]))", "dot += (e4m3_to_double(qi[t]))"),
+    "fp8_drops_v_descale": ("o[t] += p * (dv * e4m3_to_double(vj[t]));",
+                            "o[t] += p * e4m3_to_double(vj[t]);"),
+    "fp8_reference_not_power_of_two": ("const double M = quantize_p ? ceil(mx) : mx;",
+                                       "const double M = mx;"),
+    "fp8_sum_after_rounding": ("        l += exp2(x[j] - M);",
+                               "        l += quantize_p ? ldexp(e4m3_round(ldexp(exp2(x[j] - M), 7)), -7)"
+                               " : exp2(x[j] - M);"),
+    "fp8_lse_wrong_base": ("*lse = kLn2 * (M + log2(l));", "*lse = M + log(l);"),
 }
 
 
@@ -62,6 +76,7 @@ def test_planted_mistake_is_caught(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_backward_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_backward_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_fp8_pins.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutation {name} survived the oracle pins:\n{r.stdout[-2000:]}"
