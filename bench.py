@@ -12,6 +12,7 @@ of the tiled prefill kernel). Prints ONE JSON line on rank 0.
   verify    the decode-shaped split-KV path (B=16, H=32, Sq=5, Sk=4096) against
             the measured HBM bandwidth (also as a draft tree and from paged caches)
   backward  dQ, dK, dV on the same workload (2.5x the forward's FLOPs)
+  fp8       the FP8 (E4M3) forward on the same workload, against the FP8 peak
   cpu_baseline  the fp64 oracle on a bounded sample of rows, host cores
 
 --impl reference times the fp64 CPU oracle instead (the only reference arm
@@ -109,6 +110,10 @@ PREFILL_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_prefill_sm103.cu",
                    "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
 VERIFY_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_verify.cu",
                   "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
+FP8_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_prefill_fp8_sm103.cu",
+               "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
+BWD_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_backward_sm103.cu",
+               "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
 
 
 def ncu_traffic(kernel: str, sources, units_per_launch: float):
@@ -287,8 +292,41 @@ def measure_backward(w, device, sptr, args, peaks):
     tf = flops / per / 1e12
     return {"workload": w.name, "ms_per_step": per * 1e3, "TFLOP/s": tf,
             "frac_bf16_peak": tf / peaks["bf16_tflops"], "flops_per_step": flops,
-            "launches_per_step": 3, "kernels": "prep + dK/dV (4 GEMMs) + dQ (3 GEMMs)"}
+            "launches_per_step": 3, "kernels": "prep + dK/dV (4 GEMMs) + dQ (3 GEMMs)",
+            "traffic": {k: ncu_traffic(k, BWD_SOURCES, 1.0)
+                        for k in ("fa_bwd_dkdv_kernel<128>", "fa_bwd_dq_kernel<128>")}}
 
+
+def measure_fp8(w, device, sptr, args, peaks):
+    """The FP8 forward (E4M3 Q, K, V with per-tensor descales, bf16 O) on the same
+    workload and algorithmic FLOPs, against the FP8 dense peak: the measured
+    bf16 burst peak times the nominal FP8/bf16 tensor ratio of 2."""
+    from exact_tiled_attention_03_gb300 import _capi
+    from exact_tiled_attention_03_gb300.inputs import make_qkv_fp8
+
+    q8, k8, v8, ds = make_qkv_fp8(w)
+    q8, k8, v8 = (t.view(torch.uint8).to(device) for t in (q8, k8, v8))
+    o = torch.empty((w.B, w.H, w.Sq, w.d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=device)
+
+    def step():
+        st = _capi.fa_forward_fp8(q8, k8, v8, o, lse, w.B, w.H, w.Sq, w.Sk, w.d, w.causal,
+                                  w.scale, ds[0], ds[1], ds[2], sptr)
+        if st != 0:
+            raise _capi.FAError(st, "fa_forward_fp8")
+
+    for _ in range(args.warmup):
+        step()
+    n = max(10, args.steps // 2)
+    per = time_steps(step, n, torch.cuda.current_stream(device)) / n
+    _capi.check(_capi.fa_device_status(sptr), "device status after fp8")
+    tf = w.exact_flops() / per / 1e12
+    peak = 2.0 * peaks["bf16_tflops"]
+    return {"workload": w.name, "ms_per_step": per * 1e3, "TFLOP/s": tf, "peak": peak,
+            "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)",
+            "frac": tf / peak, "dtype": "e4m3 in, fp32 accumulate, bf16 out",
+            "launches_per_step": 1,
+            "traffic": ncu_traffic("fa_prefill_fp8_kernel", FP8_SOURCES, 1.0)}
 
 
 def measure_verify_variants(wv, device, sptr, args, peaks):
@@ -466,6 +504,11 @@ def run_ours(args, world, rank, local):
     if not args.no_backward:
         backward = measure_backward(w, device, sptr, args, peaks)
 
+    # the FP8 forward on the same workload
+    fp8 = None
+    if not args.no_fp8:
+        fp8 = measure_fp8(w, device, sptr, args, peaks)
+
     # the verify step's tree-mask and paged-cache forms, same bytes and roofline
     verify_ext = None
     if not args.no_verify:
@@ -497,7 +540,7 @@ def run_ours(args, world, rank, local):
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
             "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "backward": backward,
-            "cpu_baseline": cpu,
+            "fp8": fp8, "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": args.steps,  # one prefill kernel per timed step
             "gpu": torch.cuda.get_device_name(device),
@@ -520,6 +563,7 @@ def main(argv=None):
     ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

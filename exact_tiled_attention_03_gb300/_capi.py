@@ -33,6 +33,7 @@ SIGNATURES = {
     "fa_workspace_size": (_SZ, [_I64] * 5),
     "fa_forward_ws": (_I32, _ATTN + [_P, _SZ, _P]),
     "fa_prefill_forward": (_I32, _ATTN + [_P]),
+    "fa_forward_fp8": (_I32, _ATTN + [_F32, _F32, _F32, _P]),
     "fa_verify_forward": (_I32, _ATTN + [_I32, _P, _SZ, _P]),
     "fa_verify_workspace_size": (_SZ, [_I64] * 5 + [_I32]),
     "fa_verify_auto_splits": (_I32, [_I64] * 5),
@@ -48,6 +49,7 @@ SIGNATURES = {
     "fa_reference_forward_simt": (_I32, _ATTN + [_P]),
     "fa_selftest_umma": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_umma_ts": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
+    "fa_selftest_umma_f8": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_wait_timeout": (_I32, [_U64, _P]),
 }
 
@@ -125,6 +127,13 @@ def fa_forward_ws(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, workspace, ws
 def fa_prefill_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream=None) -> int:
     return load().fa_prefill_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk,
                                      d, int(bool(causal)), float(scale), _stream(stream))
+
+
+def fa_forward_fp8(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, q_descale, k_descale,
+                   v_descale, stream=None) -> int:
+    return load().fa_forward_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, d,
+                                 int(bool(causal)), float(scale), float(q_descale),
+                                 float(k_descale), float(v_descale), _stream(stream))
 
 
 def fa_verify_forward(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, n_split, workspace,
@@ -207,6 +216,11 @@ def fa_selftest_umma(a, b, c, n, k, b_mn_major, stream=None) -> int:
 def fa_selftest_umma_ts(a, b, c, n, k, b_mn_major, stream=None) -> int:
     return load().fa_selftest_umma_ts(_ptr(a), _ptr(b), _ptr(c), int(n), int(k), int(b_mn_major),
                                       _stream(stream))
+
+
+def fa_selftest_umma_f8(a, b, c, n, b_mn_major, a_tmem, stream=None) -> int:
+    return load().fa_selftest_umma_f8(_ptr(a), _ptr(b), _ptr(c), int(n), int(b_mn_major),
+                                      int(a_tmem), _stream(stream))
 
 
 def fa_selftest_wait_timeout(timeout_ns, stream=None) -> int:

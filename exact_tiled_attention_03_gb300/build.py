@@ -22,7 +22,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfa_gb300.so")
 
 SOURCES = ["fa_abi.cu", "fa_prefill_sm103.cu", "fa_verify.cu", "fa_simt.cu", "fa_selftest.cu",
-           "fa_verify_static.cu", "fa_backward_sm103.cu"]
+           "fa_verify_static.cu", "fa_backward_sm103.cu", "fa_prefill_fp8_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

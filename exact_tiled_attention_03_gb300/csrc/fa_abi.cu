@@ -225,6 +225,21 @@ bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uin
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_u8_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                       uint64_t depth, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {inner, rows, depth};
+    const cuuint64_t strides[2] = {inner, inner * rows};
+    const cuuint32_t box[3] = {128, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                          uint64_t mid, uint64_t outer, uint32_t box_rows)
 {
@@ -271,6 +286,26 @@ fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void
         return st;
     return launch_prefill_sm103(
         make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream, di->status));
+}
+
+fa_status_t fa_forward_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                           float scale, float q_descale, float k_descale, float v_descale,
+                           void *stream)
+{
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
+        return FA_ERR_INVALID_ARG;
+    if (!(q_descale > 0.0f) || !(k_descale > 0.0f) || !(v_descale > 0.0f) || d != 128)
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    if ((st = device_ok(&di)) != FA_OK)
+        return st;
+    return launch_prefill_fp8_sm103(
+        make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream, di->status),
+        q_descale, k_descale, v_descale);
 }
 
 size_t fa_verify_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
@@ -674,6 +709,22 @@ fa_status_t fa_selftest_umma_ts(const void *a, const void *b, float *c, int n, i
         return st;
     return launch_selftest_umma_ts(a, b, c, n, k, b_mn_major, static_cast<cudaStream_t>(stream),
                                    di->status);
+}
+
+fa_status_t fa_selftest_umma_f8(const void *a, const void *b, float *c, int n, int b_mn_major,
+                                int a_tmem, void *stream)
+{
+    if (!a || !b || !c || (n != 64 && n != 128) || (b_mn_major != 0 && b_mn_major != 1) ||
+        (a_tmem != 0 && a_tmem != 1) || (b_mn_major && n != 128))
+        return FA_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c))
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_umma_f8(a, b, c, n, b_mn_major, a_tmem,
+                                   static_cast<cudaStream_t>(stream), di->status);
 }
 
 fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream)

@@ -28,6 +28,12 @@ struct Problem {
 bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                          uint64_t depth, uint32_t box_rows);
 
+// Row-major [depth, rows, inner] tensor of bytes (E4M3) as a 3-D TMA map with
+// a (128 x box_rows x 1) box and 128-byte swizzle: one box spans a 128-byte
+// row. Returns false on failure.
+bool encode_tmap_u8_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                       uint64_t depth, uint32_t box_rows);
+
 // Row-major [outer, mid, rows, inner] bf16 tensor as a 4-D TMA map with a
 // (64 x box_rows x 1 x 1) box and 128-byte swizzle (K/V page pools).
 bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
@@ -59,6 +65,11 @@ fa_status_t launch_backward_sm103(const BackwardProblem &bp);
 // Launchers. Each validates nothing (fa_abi.cu does) and returns FA_OK or
 // FA_ERR_CUDA.
 fa_status_t launch_prefill_sm103(const Problem &p);
+// The FP8 forward: p.q/k/v hold E4M3 bytes, p.o bf16; d = 128 only.
+fa_status_t launch_prefill_fp8_sm103(const Problem &p, float q_descale, float k_descale,
+                                     float v_descale);
+fa_status_t launch_selftest_umma_f8(const void *a, const void *b, float *c, int n, int b_mn_major,
+                                    int a_tmem, cudaStream_t stream, unsigned int *status);
 fa_status_t launch_verify(const Problem &p, int n_split, void *workspace, size_t ws_bytes,
                           const VerifyOptions &opt = VerifyOptions());
 fa_status_t launch_reference_simt(const Problem &p);

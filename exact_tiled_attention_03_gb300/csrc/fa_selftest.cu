@@ -6,6 +6,8 @@
 //    the tests can check each encoding against a CPU matmul on its own.
 //  * fa_selftest_umma_ts_kernel: the same GEMM with A read from tensor memory
 //    (the operand form a P tile held in TMEM would use).
+//  * fa_selftest_umma_f8_kernel: the E4M3 products of the FP8 forward (A from
+//    shared or tensor memory, B K-major or MN-major).
 //  * fa_selftest_wait_kernel: the bounded mbarrier wait of the attention
 //    kernels on a barrier that nothing completes; it must give up after the
 //    limit, set the device status word and return.
@@ -189,6 +191,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, 256);
 }
 
+// The FP8 products of the E4M3 forward: C[128, N] = A[128, 128] . B with
+// .kind::f8f6f4. B is E4M3 bytes, K-major (N rows of 128) or MN-major (128
+// rows of N = 128), loaded by TMA as the attention kernel loads K and V. A is
+// either E4M3 bytes loaded the same way (a_tmem = 0), or fp32 values that
+// thread r rounds and packs with pack_e4m3x4 into TMEM columns [128, 160),
+// four per column (a_tmem = 1), the form P takes in the attention kernel.
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_selftest_umma_f8_kernel(const __grid_constant__ CUtensorMap tm_a,
+                               const __grid_constant__ CUtensorMap tm_b, const float *a_f32,
+                               float *c, int N, int b_mn_major, int a_tmem, unsigned int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + 128 * 128;
+    UmmaBars *bars = reinterpret_cast<UmmaBars *>(smem + 2 * 128 * 128);
+    const int warp = threadIdx.x / 32;
+    const int row = threadIdx.x;
+    constexpr uint32_t kColA = 128;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    if (a_tmem) {
+        uint32_t r[32];
+        for (int w = 0; w < 32; ++w) {
+            const float *x = a_f32 + row * 128 + 4 * w;
+            r[w] = pack_e4m3x4(x[0], x[1], x[2], x[3]);
+        }
+        tmem_st32(tmem + lane_base + kColA, r);
+        tmem_st_wait();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        const uint32_t b_bytes = b_mn_major ? 128u * 128u : static_cast<uint32_t>(N) * 128u;
+        mbar_arrive_expect_tx(&bars->tma, b_bytes + (a_tmem ? 0u : 128u * 128u));
+        if (!a_tmem)
+            tma_load_3d(sA, &tm_a, &bars->tma, 0, 0, 0);
+        tma_load_3d(sB, &tm_b, &bars->tma, 0, 0, 0);
+        ok = mbar_wait_drain(&bars->tma, 0, status);
+        tc_fence_after_sync();
+        if (ok) {
+            const uint32_t idesc = idesc_e4m3_f32(128, N, false, b_mn_major != 0);
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t db = b_mn_major ? smem_desc_sw128(b0 + kk * 32 * 128, 128 * 128, 1024)
+                                               : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                if (a_tmem)
+                    umma_f8_ts(tmem, tmem + kColA + kk * 8, db, idesc, kk > 0 ? 1u : 0u);
+                else
+                    umma_f8_ss(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), db, idesc,
+                               kk > 0 ? 1u : 0u);
+            }
+        }
+        umma_commit(&bars->mma);
+    }
+    __syncwarp();
+    ok = mbar_wait_drain(&bars->mma, 0, status);
+    tc_fence_after_sync();
+    for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32_wait(tmem + lane_base + c0, r);
+        if (ok)
+            for (int j = 0; j < 32; ++j)
+                c[row * N + c0 + j] = __uint_as_float(r[j]);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0)
+        tmem_dealloc(tmem, 256);
+}
+
 __global__ void fa_selftest_wait_kernel(uint64_t limit_ns, unsigned int *status)
 {
     __shared__ uint64_t bar;
@@ -239,6 +330,29 @@ fa_status_t launch_selftest_umma_ts(const void *a, const void *b, float *c, int 
         return FA_ERR_CUDA;
     selftest::fa_selftest_umma_ts_kernel<<<1, selftest::kThreads, smem, stream>>>(
         tb, static_cast<const uint32_t *>(a), c, n, k, b_mn_major, status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t launch_selftest_umma_f8(const void *a, const void *b, float *c, int n, int b_mn_major,
+                                    int a_tmem, cudaStream_t stream, unsigned int *status)
+{
+    CUtensorMap ta, tb;
+    const bool ok_b = b_mn_major ? encode_tmap_u8_3d(&tb, b, 128, 128, 1, 128)
+                                 : encode_tmap_u8_3d(&tb, b, 128, n, 1, n);
+    if (!ok_b)
+        return FA_ERR_CUDA;
+    // In the TMEM form `a` holds fp32 values and no A map is read; B's map
+    // fills the parameter.
+    if (a_tmem)
+        ta = tb;
+    else if (!encode_tmap_u8_3d(&ta, a, 128, 128, 1, 128))
+        return FA_ERR_CUDA;
+    const int smem = 2 * 128 * 128 + 64 + 1024;
+    if (cudaFuncSetAttribute(selftest::fa_selftest_umma_f8_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return FA_ERR_CUDA;
+    selftest::fa_selftest_umma_f8_kernel<<<1, selftest::kThreads, smem, stream>>>(
+        ta, tb, static_cast<const float *>(a), c, n, b_mn_major, a_tmem, status);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

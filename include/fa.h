@@ -114,6 +114,37 @@ fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void
                                int causal, float scale, void *stream);
 
 /*
+ * The FP8 forward: the FlashAttention-3 variant with 8-bit float inputs that
+ * "FlashAttention, speculative decoding, quantisation and parallelism" (The
+ * problem it solves) and "Lecture 06 — Making Decode Fast" (section 5) name.
+ * The pages give no format or recipe; this entry point takes:
+ *   q         E4M3 bytes [B, H, Sq, 128], row-major (OCP E4M3: bias 7, no
+ *             infinities, 0x7F/0xFF NaN; finite values up to 448);
+ *   k, v      E4M3 bytes [B, H, Sk, 128];
+ *   o         bf16 [B, H, Sq, 128] out;  lse  fp32 [B, H, Sq] out;
+ *   q_descale, k_descale, v_descale
+ *             one fp32 per tensor: a byte stands for descale * its E4M3 value.
+ * It computes, per row, the scores s_j = scale * q_descale * k_descale *
+ * (q . k_j) accumulated in fp32 on the FP8 tensor cores, the online softmax
+ * with an integer reference M in log2 units, weights P_j = 2^(s_j log2 e - M)
+ * rounded to E4M3 (nearest, ties to even) before O += P V runs on the FP8
+ * tensor cores, the row sum l taken before that rounding, then
+ * o = v_descale * O / l and lse = ln(sum_j e^(s_j)) (natural log; -inf and
+ * o = 0 for a row with no visible key). Because M is an integer, the
+ * rounded weights equal those rounded against the row's final max up to an
+ * exact power of two. Causal masking is bottom-right as in fa_forward.
+ * d must be 128; q, k, v, o 16-byte aligned, lse 4-byte aligned; any
+ * Sq, Sk >= 1. The caller owns every buffer; nothing is allocated.
+ * Errors: FA_ERR_INVALID_ARG for null pointers, sizes <= 0, a non-finite
+ * scale or descale; FA_ERR_UNSUPPORTED for d != 128, a scale or descale <= 0,
+ * misaligned pointers or a device other than sm_103.
+ */
+fa_status_t fa_forward_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
+                           float scale, float q_descale, float k_descale, float v_descale,
+                           void *stream);
+
+/*
  * The decode-shaped split-KV kernel (Flash-Decoding) for 1 <= Sq <= 16:
  * the keys of each (b, h) are cut into n_split contiguous chunks, one CTA
  * per (chunk, b, h) computes a partial (O_s, LSE_s), and a combine kernel

@@ -48,6 +48,18 @@ fa_status_t fa_selftest_umma_ts(const void *a, const void *b, float *c, int n, i
                                 int b_mn_major, void *stream);
 
 /*
+ * The E4M3 products of fa_forward_fp8 on one tile, with .kind::f8f6f4 MMAs:
+ *     C[128, N] = A[128, 128] . B,  B = b[N, 128]^T (b_mn_major 0, E4M3 bytes)
+ *                                  or b[128, N]     (b_mn_major 1, N = 128).
+ * a_tmem == 0: `a` is E4M3 bytes [128, 128], loaded by TMA into shared memory.
+ * a_tmem == 1: `a` is fp32 [128, 128]; each row is rounded to E4M3 and packed
+ * four per 32-bit TMEM column (element 4c + e in byte e), the MMA reading A
+ * from tensor memory. C fp32 row-major [128, N]; N in {64, 128}.
+ */
+fa_status_t fa_selftest_umma_f8(const void *a, const void *b, float *c, int n, int b_mn_major,
+                                int a_tmem, void *stream);
+
+/*
  * Launches one CTA whose thread waits, with the same bounded wait the
  * attention kernels use, on an mbarrier that nothing ever completes. After
  * `timeout_ns` nanoseconds the wait gives up and sets the device status word
