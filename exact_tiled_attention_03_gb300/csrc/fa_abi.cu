@@ -14,6 +14,10 @@
 // bounded wait gives up; fa_device_status() reads and clears it.
 __device__ unsigned int g_fa_status_word;
 
+// Work counters of the persistent prefill kernel (see fa_prefill_sm103.cu):
+// launches take slots in turn; each launch's last CTA puts its slot back to 0.
+__device__ unsigned long long g_fa_work_slots[2 * fa::kWorkSlots];
+
 namespace fa {
 namespace {
 
@@ -24,6 +28,7 @@ struct DeviceInfo {
     int num_sms = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned int *status = nullptr;
+    unsigned long long *work = nullptr;
 };
 
 std::mutex g_mu;
@@ -47,6 +52,9 @@ const DeviceInfo *device_info()
         if (cudaGetSymbolAddress(&addr, g_fa_status_word) != cudaSuccess)
             return nullptr;
         di.status = static_cast<unsigned int *>(addr);
+        if (cudaGetSymbolAddress(&addr, g_fa_work_slots) != cudaSuccess)
+            return nullptr;
+        di.work = static_cast<unsigned long long *>(addr);
         di.ready = true;
     }
     return &di;
@@ -114,6 +122,9 @@ Problem make_problem(const void *q, const void *k, const void *v, void *o, float
     p.scale = scale;
     p.stream = static_cast<cudaStream_t>(stream);
     p.status = status;
+    const DeviceInfo *di = device_info();  // already looked up by the caller's device_ok()
+    p.num_sms = di ? di->num_sms : 0;
+    p.work_slots = di ? di->work : nullptr;
     return p;
 }
 

@@ -418,6 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           r, half, 2);
         }
     }
+    // Threads that issued TMA stores wait for their writes (not only for the
+    // shared-memory reads) before the CTA exits, so that the next kernel in the
+    // stream reads them.
+    tma_store_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -493,7 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *abort_flag = &bars->abort_flag;
 
     if (warp == kProducerWarp) {
-        if (lane == 0) {
+        // A query tile that sees no key tile loads nothing: its epilogue
+        // stages the zero dQ tile in Q's buffer, which a late load would
+        // overwrite.
+        if (lane == 0 && n_kv > 0) {
             mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTile);
             for (int b = 0; b < D / 64; ++b) {
                 tma_load_3d(smem + C::kOffQ + b * kBoxBytes, &tm_q, &bars->q_full, b * 64, q0, bh);
@@ -649,6 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_tile<D>(tmem + lane_base + C::kColDQ, p.scale, n_kv > 0, smem + C::kOffQ,
                           &tm_dq, q0, bh, r, half, 2);
     }
+    // Threads that issued TMA stores wait for their writes (not only for the
+    // shared-memory reads) before the CTA exits, so that the next kernel in the
+    // stream reads them.
+    tma_store_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();

@@ -21,7 +21,13 @@ struct Problem {
     float scale;
     cudaStream_t stream;
     unsigned int *status;  // device status word (timeouts)
+    int num_sms;           // SMs of the current device
+    // Library-owned work counters of the persistent prefill kernel: kWorkSlots
+    // pairs (next item, finished CTAs), all zero between launches.
+    unsigned long long *work_slots;
 };
+
+constexpr int kWorkSlots = 1024;
 
 // Row-major [depth, rows, inner] bf16 tensor as a 3-D TMA map with a
 // (64 x box_rows x 1) box and 128-byte swizzle. Returns false on failure.

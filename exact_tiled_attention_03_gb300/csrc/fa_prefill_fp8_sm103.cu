@@ -466,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // Threads that issued TMA stores wait for their writes (not only for the
+    // shared-memory reads) before the CTA exits, so that the next kernel in the
+    // stream reads them.
+    tma_store_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();

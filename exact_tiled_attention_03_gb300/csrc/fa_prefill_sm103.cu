@@ -11,11 +11,15 @@
 // (LSE = m + ln l).
 //
 // The GB300 shape of it (not the pages' SRAM/Hopper design):
-//   * one CTA per SM owns two 128-row query tiles of one (batch, head);
-//     both share every K/V tile it loads;
-//   * warp 8 (producer) moves Q once and then K_j, V_j through a ring of
-//     shared-memory stages with TMA (128-byte swizzle), one mbarrier pair per
-//     stage;
+//   * persistent: one CTA per SM takes work items from a launch-wide counter
+//     until none is left. An item is two 128-row query tiles of one
+//     (batch, head); both share every K/V tile the CTA loads;
+//   * warp 8 (producer) takes the items (in the order decode_item gives),
+//     publishes each to the other warps
+//     through a small shared-memory queue, and moves its Q tiles and then
+//     K_j, V_j through a ring of shared-memory stages with TMA (128-byte
+//     swizzle), one mbarrier pair per stage. The next item's first loads and
+//     S MMAs run while the softmax warps finish the current item;
 //   * warp 9 (one elected thread) issues tcgen05.mma: S_t = Q_t K_j^T into
 //     tensor memory (TMEM), and O_t += P_t V_j with P_t read from TMEM and V
 //     read MN-major straight from its row-major tile; completion is signalled
@@ -29,10 +33,14 @@
 //     max exceeds the reference by more than 2^8 (or on the row's first
 //     tile) does it recompute the row against the new max and rescale its O
 //     row in TMEM. It then writes P (bf16) over its S row in TMEM. At the end
-//     it divides by l, writes the bf16 O row into shared memory for a TMA
-//     store and writes its LSE.
+//     of an item it divides by l and writes its bf16 O row into the tile's
+//     own staging box in shared memory, 64 columns at a time, each box sent
+//     by one TMA store; then it writes its LSE. Q's buffers are reloaded for
+//     the next item as soon as the item's MMAs are done.
 // Every wait is bounded; on expiry the CTA stops, drains what it has in
 // flight, frees its tensor memory and sets the device status word.
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -62,12 +70,17 @@ template <int D>
 struct Cfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kTileBytes = kBlockM * D * 2;  // Q, K, V or O tile
-    static constexpr int kStages = (D == 128) ? 5 : 10;  // ~160 KB of K/V ring
+    // K/V ring: 128-160 KB. At d = 128, 4 stages measured as fast as 5, and
+    // the freed 32 KB hold the O staging boxes.
+    static constexpr int kStages = (D == 128) ? 4 : 10;
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kTiles * kTileBytes;
-    static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+    // One 128-row x 64-column bf16 box per tile for staging O to its TMA store.
+    static constexpr int kOffOut = kOffKV + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffOut + kTiles * kBoxBytes;
     static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     // S_t in columns [128 t, 128 t + 128); P_t (bf16, two per column) is
     // written over the first 64 columns of S_t once S_t is in registers.
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
@@ -76,22 +89,32 @@ struct Cfg {
 };
 
 struct Params {
-    int Sq, Sk, BH, n_qblk;
+    int Sq, Sk, BH, n_qblk, n_items, heads_per_group;
     int causal;
     float scale;       // softmax scale
     float scale_log2;  // scale * log2(e)
+    __nv_bfloat16 *o;
     float *lse;
     unsigned int *status;
+    unsigned long long *work;  // this launch's (next item, finished CTAs) pair
 };
 
+// Work-item queue slots. The consumers release a slot when they have finished
+// its item, so the producer holds at most one item beyond the running one
+// (more would let a CTA hoard short items at the end of the launch).
+constexpr int kQueue = 2;
+
 struct Bars {
-    uint64_t q_full;
+    uint64_t q_full[kTiles];   // Q_t of the current item landed (one phase per item with keys)
     uint64_t s_full[kTiles];   // S_t(j) in TMEM (one phase per key tile)
     uint64_t p_full[kTiles];   // P_t(j) in TMEM and O_t rescaled (one phase per key tile)
-    uint64_t o_done[kTiles];   // last O_t += P_t V completed (one phase)
+    uint64_t o_done[kTiles];   // last O_t += P_t V completed (one phase per item with keys)
+    uint64_t item_full[kQueue];
+    uint64_t item_empty[kQueue];
     uint64_t drain;
     uint64_t kv_full[16];
     uint64_t kv_empty[16];
+    int items[kQueue];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -104,6 +127,48 @@ __device__ __forceinline__ int visible_keys(int i, int Sq, int Sk, int causal)
         return Sk;
     int n = i + (Sk - Sq) + 1;
     return n < 0 ? 0 : (n > Sk ? Sk : n);
+}
+
+// Work item w: two query tiles of one (batch, head). Heads are taken in
+// groups of heads_per_group (the last group may be smaller); within a group
+// the query blocks go heaviest first (last block, most keys under the causal
+// mask), across all the group's heads. One head per group is head-major
+// order: items handed out together share a few heads' K/V in L2.
+struct Item {
+    int bh;
+    int q0[kTiles], n_kv[kTiles], mask_from[kTiles];
+    int n_kv_max;
+};
+
+__device__ __forceinline__ Item decode_item(int w, const Params &p)
+{
+    Item it;
+    const int per_group = p.heads_per_group * p.n_qblk;
+    const int g = w / per_group, rg = w % per_group;
+    const int hg = min(p.heads_per_group, p.BH - g * p.heads_per_group);
+    it.bh = g * p.heads_per_group + rg % hg;
+    const int qblk = p.n_qblk - 1 - rg / hg;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        it.q0[t] = qblk * (kTiles * kBlockM) + t * kBlockM;
+        if (it.q0[t] < p.Sq) {
+            const int last = min(it.q0[t] + kBlockM - 1, p.Sq - 1);
+            it.n_kv[t] = (visible_keys(last, p.Sq, p.Sk, p.causal) + kBlockN - 1) / kBlockN;
+            it.mask_from[t] = visible_keys(it.q0[t], p.Sq, p.Sk, p.causal) / kBlockN;
+        } else {
+            it.n_kv[t] = 0;
+            it.mask_from[t] = 0;
+        }
+    }
+    it.n_kv_max = max(it.n_kv[0], it.n_kv[1]);
+    return it;
+}
+
+// The next work item of this launch, or -1 when none is left.
+__device__ __forceinline__ int grab_item(const Params &p)
+{
+    const unsigned long long w = atomicAdd(p.work, 1ull);
+    return w < static_cast<unsigned long long>(p.n_items) ? static_cast<int>(w) : -1;
 }
 
 template <int D>
@@ -125,34 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // Head-major order, heaviest query block first within each head: the CTAs
-    // running at the same time share a few heads' K/V in L2, and with the
-    // causal mask the last query blocks (most keys) start first.
-    const int bh = static_cast<int>(blockIdx.x / p.n_qblk);
-    const int qblk = p.n_qblk - 1 - static_cast<int>(blockIdx.x % p.n_qblk);
-
-    int q0[kTiles], n_kv[kTiles], mask_from[kTiles];
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-        q0[t] = qblk * (kTiles * kBlockM) + t * kBlockM;
-        if (q0[t] < p.Sq) {
-            const int last = min(q0[t] + kBlockM - 1, p.Sq - 1);
-            n_kv[t] = (visible_keys(last, p.Sq, p.Sk, p.causal) + kBlockN - 1) / kBlockN;
-            mask_from[t] = visible_keys(q0[t], p.Sq, p.Sk, p.causal) / kBlockN;
-        } else {
-            n_kv[t] = 0;
-            mask_from[t] = 0;
-        }
-    }
-    const int n_kv_max = max(n_kv[0], n_kv[1]);
-    const bool any_tile = q0[0] < p.Sq;
-
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 1);
         for (int t = 0; t < kTiles; ++t) {
+            mbar_init(&bars->q_full[t], 1);
             mbar_init(&bars->s_full[t], 1);
             mbar_init(&bars->p_full[t], 4);
             mbar_init(&bars->o_done[t], 1);
+        }
+        for (int s = 0; s < kQueue; ++s) {
+            mbar_init(&bars->item_full[s], 1);
+            mbar_init(&bars->item_empty[s], 1 + kSoftmaxWarps);  // MMA thread + softmax warps
         }
         mbar_init(&bars->drain, 1);
         for (int s = 0; s < C::kStages; ++s) {
@@ -180,50 +227,84 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && any_tile) {
+        // Takes work items from the launch's counter, publishes each to the
+        // other roles through the item queue, then loads its Q tiles and its
+        // K_j, V_j through the ring. Items run back to back: the next item's
+        // first K/V tiles and Q tiles load while the current one finishes.
+        if (lane == 0) {
             const uint64_t pol_stream = l2_policy_evict_first();  // Q: read once
             const uint64_t pol_keep = l2_policy_evict_last();     // K/V: re-read by other q-blocks
-            uint32_t q_bytes = 0;
-            for (int t = 0; t < kTiles; ++t)
-                if (q0[t] < p.Sq)
-                    q_bytes += C::kTileBytes;
-            mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-            for (int t = 0; t < kTiles; ++t)
-                if (q0[t] < p.Sq)
-                    for (int b = 0; b < C::kBoxes; ++b)
-                        tma_load_3d_hint(sQ + t * C::kTileBytes + b * kBoxBytes, &tm_q,
-                                         &bars->q_full, b * 64, q0[t], bh, pol_stream);
-            int it = 0;
+            int it = 0;                       // ring index, continuous across items
+            uint32_t q_loads[kTiles] = {0, 0};  // q_full phases started
+            bool q_busy[kTiles] = {false, false};  // Q_t still read by the last item's MMAs
+            uint32_t o_phases[kTiles] = {0, 0};    // o_done phases of items with keys
             bool ok = true;
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                for (int which = 0; which < 2 && ok; ++which, ++it) {
-                    const int s = it % C::kStages;
-                    const uint32_t use = it / C::kStages;
-                    if (use > 0 &&
-                        !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status)) {
+            auto load_kv = [&](int j, int which, int bh) {
+                const int s = it % C::kStages;
+                const uint32_t use = it / C::kStages;
+                if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status))
+                    return false;
+                mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
+                const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d_hint(sKV + s * C::kTileBytes + b * kBoxBytes, tm, &bars->kv_full[s],
+                                     b * 64, j * kBlockN, bh, pol_keep);
+                ++it;
+                return true;
+            };
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kQueue;
+                if (n >= kQueue &&
+                    !mbar_wait(&bars->item_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status))
+                    break;
+                const int w = grab_item(p);
+                bars->items[slot] = w;
+                mbar_arrive(&bars->item_full[slot]);  // release: the consumers read items[slot]
+                if (w < 0)
+                    break;
+                const Item I = decode_item(w, p);
+                if (I.n_kv_max == 0)
+                    continue;
+                // K_0 and V_0 first: they do not wait for the Q buffers.
+                ok = load_kv(0, 0, I.bh) && load_kv(0, 1, I.bh);
+                for (int t = 0; t < kTiles && ok; ++t) {
+                    if (I.n_kv[t] == 0)
+                        continue;
+                    // Q_t's buffer is free once the previous item's last MMA on
+                    // tile t has completed.
+                    if (q_busy[t] &&
+                        !mbar_wait(&bars->o_done[t], (o_phases[t] - 1) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
-                    const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
+                    mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
                     for (int b = 0; b < C::kBoxes; ++b)
-                        tma_load_3d_hint(sKV + s * C::kTileBytes + b * kBoxBytes, tm,
-                                         &bars->kv_full[s], b * 64, j * kBlockN, bh, pol_keep);
+                        tma_load_3d_hint(sQ + t * C::kTileBytes + b * kBoxBytes, &tm_q,
+                                         &bars->q_full[t], b * 64, I.q0[t], I.bh, pol_stream);
+                    ++q_loads[t];
+                    q_busy[t] = true;
+                    ++o_phases[t];
                 }
+                for (int j = 1; j < I.n_kv_max && ok; ++j)
+                    ok = load_kv(j, 0, I.bh) && load_kv(j, 1, I.bh);
             }
             // Drain: every load issued must have landed before the CTA exits.
-            mbar_wait_drain(&bars->q_full, 0, p.status);
+            for (int t = 0; t < kTiles; ++t)
+                if (q_loads[t] > 0)
+                    mbar_wait_drain(&bars->q_full[t], (q_loads[t] - 1) & 1, p.status);
             for (int k = max(0, it - C::kStages); k < it; ++k)
                 mbar_wait_drain(&bars->kv_full[k % C::kStages], (k / C::kStages) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Ring order of the loads: K_0, V_0, K_1, V_1, ... (K_j at index 2j,
-        // V_j at 2j+1), consumed in the same order. Issue order: S_0(0), S_1(0),
-        // then per j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites
-        // the TMEM columns that held P_t(j); the tensor pipe executes one
-        // thread's MMAs in order, so PV_t(j) has read P_t(j) by then.
-        if (lane == 0 && any_tile && n_kv_max > 0) {
+        // Per item, ring order of the loads: K_0, V_0, K_1, V_1, ... (K_j at
+        // index 2j, V_j at 2j+1 from the item's first ring index), consumed in
+        // the same order. Issue order: S_0(0), S_1(0), then per j: PV_0(j),
+        // S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites the TMEM columns
+        // that held P_t(j), and the next item's PV_t(0) overwrites O_t; the
+        // tensor pipe executes one thread's MMAs in order, and the softmax
+        // warps have read O_t (epilogue) before they publish the next P_t.
+        if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
             const uint32_t colS[kTiles] = {C::kColS0, C::kColS1};
@@ -244,66 +325,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_bf16_ss(tmem + colS[t], a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
                 }
             };
-            // One 64-key half of O_t += P_t V_j (k-steps 4h .. 4h+3).
-            auto issue_pv_half = [&](int t, int slot, int j, int h) {
+            auto issue_pv = [&](int t, int slot, int j) {
                 const uint64_t b0 = dv0 + kTileStep * slot;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int kk = 4 * h + q;
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
                     umma_bf16_ts(tmem + colO[t], tmem + colS[t] + kk * 8,
                                  b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
                                  (j > 0 || kk > 0) ? 1u : 0u);
-                }
             };
             auto ring_wait = [&](int idx) {
                 return mbar_wait(&bars->kv_full[idx % C::kStages], (idx / C::kStages) & 1,
                                  abort_flag, p.status);
             };
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status) && ring_wait(0);  // K_0
-            if (ok) {
-                tc_fence_after_sync();
-                for (int t = 0; t < kTiles; ++t)
-                    if (n_kv[t] > 0) {
-                        issue_s(t, 0);
-                        umma_commit(&bars->s_full[t]);
-                    }
-                umma_commit(&bars->kv_empty[0]);
-            }
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                const int iv = 2 * j + 1, ik = 2 * j + 2;
-                ok = ring_wait(iv);  // V_j
-                if (!ok)
+            int it = 0;
+            uint32_t q_waits[kTiles] = {0, 0}, p_waits[kTiles] = {0, 0};
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kQueue;
+                if (!mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status))
                     break;
-                tc_fence_after_sync();
-                bool k_ready = false;
+                const int w = bars->items[slot];
+                if (w < 0)
+                    break;
+                const Item I = decode_item(w, p);
+                if (I.n_kv_max == 0) {
+                    mbar_arrive(&bars->item_empty[slot]);
+                    continue;
+                }
+                // S_t(0) as soon as Q_t is in: tile 0's Q buffer frees a key
+                // tile earlier than tile 1's at the end of a causal item.
+                ok = ring_wait(it);  // K_0
                 for (int t = 0; t < kTiles && ok; ++t) {
-                    if (j >= n_kv[t])
+                    if (I.n_kv[t] == 0)
                         continue;
-                    ok = mbar_wait(&bars->p_full[t], j & 1, abort_flag, p.status);
+                    ok = mbar_wait(&bars->q_full[t], (q_waits[t]++) & 1, abort_flag, p.status);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
-                    issue_pv_half(t, iv % C::kStages, j, 0);
-                    issue_pv_half(t, iv % C::kStages, j, 1);
-                    if (j + 1 < n_kv[t]) {
-                        if (!k_ready) {
-                            ok = ring_wait(ik);  // K_{j+1}
-                            if (!ok)
-                                break;
-                            tc_fence_after_sync();
-                            k_ready = true;
-                        }
-                        issue_s(t, ik % C::kStages);
-                        umma_commit(&bars->s_full[t]);
-                    } else {
-                        umma_commit(&bars->o_done[t]);  // this tile's last PV
-                    }
+                    issue_s(t, it % C::kStages);
+                    umma_commit(&bars->s_full[t]);
                 }
                 if (!ok)
                     break;
-                umma_commit(&bars->kv_empty[iv % C::kStages]);
-                if (k_ready)
-                    umma_commit(&bars->kv_empty[ik % C::kStages]);
+                umma_commit(&bars->kv_empty[it % C::kStages]);
+                for (int j = 0; j < I.n_kv_max && ok; ++j) {
+                    const int iv = it + 2 * j + 1, ik = it + 2 * j + 2;
+                    ok = ring_wait(iv);  // V_j
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    bool k_ready = false;
+                    for (int t = 0; t < kTiles && ok; ++t) {
+                        if (j >= I.n_kv[t])
+                            continue;
+                        ok = mbar_wait(&bars->p_full[t], (p_waits[t]++) & 1, abort_flag, p.status);
+                        if (!ok)
+                            break;
+                        tc_fence_after_sync();
+                        issue_pv(t, iv % C::kStages, j);
+                        if (j + 1 < I.n_kv[t]) {
+                            if (!k_ready) {
+                                ok = ring_wait(ik);  // K_{j+1}
+                                if (!ok)
+                                    break;
+                                tc_fence_after_sync();
+                                k_ready = true;
+                            }
+                            issue_s(t, ik % C::kStages);
+                            umma_commit(&bars->s_full[t]);
+                        } else {
+                            umma_commit(&bars->o_done[t]);  // this tile's last PV of the item
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    umma_commit(&bars->kv_empty[iv % C::kStages]);
+                    if (k_ready)
+                        umma_commit(&bars->kv_empty[ik % C::kStages]);
+                }
+                it += 2 * I.n_kv_max;
+                mbar_arrive(&bars->item_empty[slot]);  // every MMA of the item is issued
             }
             // Drain: all MMAs issued by this thread complete before TMEM is freed.
             umma_commit(&bars->drain);
@@ -314,202 +415,255 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp / 4;              // query tile of this warpgroup
         const int wq = warp % 4;             // TMEM lane quarter of this warp
         const int r = wq * 32 + lane;        // row within the tile
-        const int i = q0[t] + r;             // query row
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
         const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
-        uint8_t *sOut = sQ + t * C::kTileBytes;  // Q_t's buffer, reused for the O tile
-        const uint32_t sOut_a = smem_u32(sOut);
-        const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
         const float sl2 = p.scale_log2;
-
-        // m: the reference max of this row's exponentials (raw score units,
-        // scale > 0). It is updated lazily: only when a tile's max exceeds it by
-        // more than 2^kRescaleLog2 in the exponent (or on the first visible key).
-        // O and l always share the same reference, so the result stays exact,
-        // and P = 2^((s - m) * sl2) stays <= 2^kRescaleLog2.
-        float m = -INFINITY;
-        float l = 0.0f;       // running sum of 2^((s - m) * sl2)
-        bool ok = true;
-        if (q0[t] < p.Sq)
-            ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
-        // Waits feed .sync.aligned TMEM instructions: keep their outcome warp-uniform.
-        ok = __all_sync(0xffffffffu, ok);
-
         const float2 sl2x2 = make_float2(sl2, sl2);
-        for (int j = 0; j < n_kv[t] && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort_flag, p.status));
-            if (!ok)
+        uint32_t s_waits = 0, o_waits = 0;  // phases of s_full[t] and o_done[t] consumed
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            const int slot = n % kQueue;
+            // Waits feed .sync.aligned TMEM instructions: keep their outcome
+            // warp-uniform. The tile's 4 warps also leave the loop together
+            // (their epilogue has named barriers), so the outcome is made
+            // tile-uniform here.
+            const bool got_item = __all_sync(
+                0xffffffffu,
+                mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status));
+            if (named_bar_or(1 + t, 128, !got_item))
                 break;
-            tc_fence_after_sync();
-            const bool masked_tile = j >= mask_from[t];
-            const int key0 = j * kBlockN;
-            uint32_t pk[kBlockN / 2];
-            float2 acc[4];
-            // One pass over S_t in chunks of kChunk columns: load, mask, and (when
-            // `with_exp`) p = 2^(s*sl2 + neg), accumulated into acc and packed
-            // into pk. Returns the max of the raw scores it saw.
-            auto pass = [&](bool with_exp, float neg) {
-                const float2 negx2 = make_float2(neg, neg);
-                float mx = -INFINITY;
+            const int w = *reinterpret_cast<volatile int *>(&bars->items[slot]);
+            if (w < 0)
+                break;
+            // The item's slot is released when this warp has finished the item.
+            auto release = [&]() {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->item_empty[slot]);
+            };
+            const Item I = decode_item(w, p);
+            const int q0 = I.q0[t], n_kv = I.n_kv[t], mask_from = I.mask_from[t];
+            const int i = q0 + r;  // query row
+            const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
+
+            // m: the reference max of this row's exponentials (raw score units,
+            // scale > 0). It is updated lazily: only when a tile's max exceeds it
+            // by more than 2^kRescaleLog2 in the exponent (or on the first
+            // visible key). O and l always share the same reference, so the
+            // result stays exact, and P = 2^((s - m) * sl2) stays <= 2^kRescaleLog2.
+            float m = -INFINITY;
+            float l = 0.0f;  // running sum of 2^((s - m) * sl2)
+            for (int j = 0; j < n_kv && ok; ++j) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], (s_waits++) & 1,
+                                                       abort_flag, p.status));
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                const bool masked_tile = j >= mask_from;
+                const int key0 = j * kBlockN;
+                uint32_t pk[kBlockN / 2];
+                float2 acc[4];
+                // One pass over S_t in chunks of kChunk columns: load, mask, and
+                // (when `with_exp`) p = 2^(s*sl2 + neg), accumulated into acc and
+                // packed into pk. Returns the max of the raw scores it saw.
+                auto pass = [&](bool with_exp, float neg) {
+                    const float2 negx2 = make_float2(neg, neg);
+                    float mx = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    acc[q] = make_float2(0.f, 0.f);
-                // Process one chunk of kChunk scores starting at column c0.
-                auto consume = [&](const uint32_t *raw, int c0) {
-                    float sv[kChunk];
-#pragma unroll
-                    for (int c = 0; c < kChunk; ++c)
-                        sv[c] = __uint_as_float(raw[c]);
-                    if (masked_tile) {
+                    for (int q = 0; q < 4; ++q)
+                        acc[q] = make_float2(0.f, 0.f);
+                    // Process one chunk of kChunk scores starting at column c0.
+                    auto consume = [&](const uint32_t *raw, int c0) {
+                        float sv[kChunk];
 #pragma unroll
                         for (int c = 0; c < kChunk; ++c)
-                            if (key0 + c0 + c >= lim)
-                                sv[c] = -INFINITY;
-                    }
-                    float part[kChunk / 16];
+                            sv[c] = __uint_as_float(raw[c]);
+                        if (masked_tile) {
 #pragma unroll
-                    for (int k = 0; k < kChunk / 16; ++k) {
-                        float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
-#pragma unroll
-                        for (int e = 3; e < 15; e += 2)
-                            x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
-                        part[k] = fmaxf(x, sv[16 * k + 15]);
-                    }
-#pragma unroll
-                    for (int k = 0; k < kChunk / 16; ++k)
-                        mx = fmaxf(mx, part[k]);
-                    if (with_exp) {
-#pragma unroll
-                        for (int c = 0; c < kChunk / 2; ++c) {
-                            const float2 x = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2);
-                            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                            acc[c % 4] = fadd2(acc[c % 4], e);
-                            pk[c0 / 2 + c] = pack_bf16x2(e.x, e.y);
+                            for (int c = 0; c < kChunk; ++c)
+                                if (key0 + c0 + c >= lim)
+                                    sv[c] = -INFINITY;
                         }
+                        float part[kChunk / 16];
+#pragma unroll
+                        for (int k = 0; k < kChunk / 16; ++k) {
+                            float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
+#pragma unroll
+                            for (int e = 3; e < 15; e += 2)
+                                x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
+                            part[k] = fmaxf(x, sv[16 * k + 15]);
+                        }
+#pragma unroll
+                        for (int k = 0; k < kChunk / 16; ++k)
+                            mx = fmaxf(mx, part[k]);
+                        if (with_exp) {
+#pragma unroll
+                            for (int c = 0; c < kChunk / 2; ++c) {
+                                const float2 x = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2x2,
+                                                       negx2);
+                                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                                acc[c % 4] = fadd2(acc[c % 4], e);
+                                pk[c0 / 2 + c] = pack_bf16x2(e.x, e.y);
+                            }
+                        }
+                    };
+#pragma unroll
+                    for (int c0 = 0; c0 < kBlockN; c0 += kChunk) {
+                        uint32_t raw[kChunk];
+                        tmem_ld64_wait(tS + c0, raw);
+                        consume(raw, c0);
                     }
+                    return mx;
                 };
+                // Speculative pass: when every lane already has a reference max,
+                // the exponentials are computed against it while the tile's max
+                // is found.
+                const bool spec = __all_sync(0xffffffffu, m != -INFINITY);
+                const float mx = pass(spec, spec ? -m * sl2 : 0.0f);
+                // The reference moves only when the tile's max exceeds it by more
+                // than 2^kRescaleLog2 (or on the first visible key); O and l always
+                // share it, so the result stays exact and P stays <= 2^kRescaleLog2.
+                // NaN (both -inf) compares false: nothing visible yet, keep m.
+                const float m_new = fmaxf(m, mx);
+                const bool move = (m_new - m) * sl2 > kRescaleLog2;
+                const float m_use = move ? m_new : m;
+                const float corr = move ? ex2_approx((m - m_use) * sl2) : 1.0f;  // 0 when m = -inf
+                if (!spec || __any_sync(0xffffffffu, move)) {
+                    // Second pass with the moved reference (lanes that did not move
+                    // recompute the same values). S_t is still intact: P has not
+                    // been written yet.
+                    pass(true, (m_use == -INFINITY) ? 0.0f : -m_use * sl2);
+                    // O_t *= corr (warp-uniform; lanes that did not move multiply
+                    // by 1). PV_t(j-1) has completed: S_t(j), committed after it,
+                    // is done.
+                    if (j > 0 && __any_sync(0xffffffffu, move)) {
+                        const float2 cx2 = make_float2(corr, corr);
 #pragma unroll
-                for (int c0 = 0; c0 < kBlockN; c0 += kChunk) {
-                    uint32_t raw[kChunk];
-                    tmem_ld64_wait(tS + c0, raw);
-                    consume(raw, c0);
-                }
-                return mx;
-            };
-            // Speculative pass: when every lane already has a reference max, the
-            // exponentials are computed against it while the tile's max is found.
-            const bool spec = __all_sync(0xffffffffu, m != -INFINITY);
-            const float mx = pass(spec, spec ? -m * sl2 : 0.0f);
-            // The reference moves only when the tile's max exceeds it by more
-            // than 2^kRescaleLog2 (or on the first visible key); O and l always
-            // share it, so the result stays exact and P stays <= 2^kRescaleLog2.
-            // NaN (both -inf) compares false: nothing visible yet, keep m.
-            const float m_new = fmaxf(m, mx);
-            const bool move = (m_new - m) * sl2 > kRescaleLog2;
-            const float m_use = move ? m_new : m;
-            const float corr = move ? ex2_approx((m - m_use) * sl2) : 1.0f;  // 0 when m = -inf
-            if (!spec || __any_sync(0xffffffffu, move)) {
-                // Second pass with the moved reference (lanes that did not move
-                // recompute the same values). S_t is still intact: P has not
-                // been written yet.
-                pass(true, (m_use == -INFINITY) ? 0.0f : -m_use * sl2);
-                // O_t *= corr (warp-uniform; lanes that did not move multiply by
-                // 1). PV_t(j-1) has completed: S_t(j), committed after it, is done.
-                if (j > 0 && __any_sync(0xffffffffu, move)) {
-                    const float2 cx2 = make_float2(corr, corr);
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32_wait(tO + c0, o);
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32_wait(tO + c0, o);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
-                                                               __uint_as_float(o[2 * c + 1])),
-                                                   cx2);
-                            o[2 * c] = __float_as_uint(v.x);
-                            o[2 * c + 1] = __float_as_uint(v.y);
+                            for (int c = 0; c < 16; ++c) {
+                                const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
+                                                                   __uint_as_float(o[2 * c + 1])),
+                                                       cx2);
+                                o[2 * c] = __float_as_uint(v.x);
+                                o[2 * c + 1] = __float_as_uint(v.y);
+                            }
+                            tmem_st32(tO + c0, o);
                         }
-                        tmem_st32(tO + c0, o);
                     }
                 }
-            }
-            // P (bf16 pairs) over S_t's first 64 columns, then publish.
-            {
-                uint32_t lo[32], hi[32];
+                // P (bf16 pairs) over S_t's first 64 columns, then publish.
+                {
+                    uint32_t lo[32], hi[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    lo[c] = pk[c];
-                    hi[c] = pk[32 + c];
+                    for (int c = 0; c < 32; ++c) {
+                        lo[c] = pk[c];
+                        hi[c] = pk[32 + c];
+                    }
+                    tmem_st32(tS, lo);
+                    tmem_st32(tS + 32, hi);
                 }
-                tmem_st32(tS, lo);
-                tmem_st32(tS + 32, hi);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->p_full[t]);
+                const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+                const float2 a = fadd2(a01, a23);
+                l = l * corr + (a.x + a.y);
+                m = m_use;
             }
-            tmem_st_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars->p_full[t]);
-            const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
-            const float2 a = fadd2(a01, a23);
-            l = l * corr + (a.x + a.y);
-            m = m_use;
-        }
 
-        // ------------------------------------------------------------ epilogue
-        if (ok && q0[t] < p.Sq) {
-            if (n_kv[t] > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], 0, abort_flag, p.status));
-                tc_fence_after_sync();
+            // -------------------------------------------------------- epilogue
+            // O / l into this tile's staging box (swizzled like the TMA box), one
+            // 64-column box at a time, each sent by a TMA store, then the LSE.
+            // The next item's P_t is published only after these TMEM reads, so
+            // its PV_t(0) cannot overwrite O_t early.
+            if (q0 >= p.Sq) {
+                release();
+                continue;
             }
-            if (ok) {
-                const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+            bool got = ok;
+            if (got && n_kv > 0) {
+                got = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (o_waits++) & 1,
+                                                        abort_flag, p.status));
+                if (got)
+                    tc_fence_after_sync();
+            }
+            // The tile's 4 warps take the barriers below together or not at all.
+            if (named_bar_or(1 + t, 128, !got)) {
+                ok = false;
+                break;
+            }
+            const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+            uint8_t *sOut = smem + C::kOffOut + t * kBoxBytes;
+            const uint32_t sOut_a = smem_u32(sOut);
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int b = 0; b < C::kBoxes; ++b) {
+                if (b > 0)
+                    named_bar_sync(1 + t, 128);  // the previous box has been read out
+#pragma unroll
+                for (int c1 = 0; c1 < 64; c1 += 32) {
+                    const int c0 = 64 * b + c1;
                     uint32_t o[32];
-                    if (n_kv[t] > 0) {
+                    if (n_kv > 0) {
                         tmem_ld32_wait(tO + c0, o);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
                             o[c] = 0u;
                     }
-                    uint32_t pk[16];
+                    uint32_t pko[16];
 #pragma unroll
                     for (int c = 0; c < 32; c += 2)
-                        pk[c / 2] = pack_bf16x2(__uint_as_float(o[c]) * inv_l,
-                                                __uint_as_float(o[c + 1]) * inv_l);
-                    const int box = c0 / 64;
+                        pko[c / 2] = pack_bf16x2(__uint_as_float(o[c]) * inv_l,
+                                                 __uint_as_float(o[c + 1]) * inv_l);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint32_t chunk = ((c0 % 64) / 8) + q;
-                        st_shared_v4(sOut_a + box * kBoxBytes +
-                                         sw128_offset(static_cast<uint32_t>(r), chunk),
-                                     pk[q * 4], pk[q * 4 + 1], pk[q * 4 + 2], pk[q * 4 + 3]);
+                        const uint32_t chunk = (c1 / 8) + q;
+                        st_shared_v4(sOut_a + sw128_offset(static_cast<uint32_t>(r), chunk),
+                                     pko[q * 4], pko[q * 4 + 1], pko[q * 4 + 2], pko[q * 4 + 3]);
                     }
                 }
-                if (i < p.Sq) {
-                    const float lse = (l > 0.0f) ? m * p.scale + logf(l) : -INFINITY;
-                    p.lse[static_cast<size_t>(bh) * p.Sq + i] = lse;
+                fence_proxy_async_smem();
+                named_bar_sync(1 + t, 128);
+                if (r == 0) {
+                    tma_store_3d(&tm_o, sOut, b * 64, q0, I.bh);
+                    tma_store_commit();
+                    // The box may be rewritten (next box, or the next item after
+                    // the tile's next barrier); the writes finish on their own.
+                    tma_store_wait_read_all();
                 }
             }
-        }
-        tc_fence_before_sync();
-        fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
-        if (r == 0 && ok && q0[t] < p.Sq && !*reinterpret_cast<volatile int *>(abort_flag)) {
-            for (int b = 0; b < C::kBoxes; ++b)
-                tma_store_3d(&tm_o, sOut + b * kBoxBytes, b * 64, q0[t], bh);
-            tma_store_commit();
-            tma_store_wait_read_all();  // the staging buffer may go; the writes finish on their own
+            if (i < p.Sq) {
+                const float lse = (l > 0.0f) ? m * p.scale + logf(l) : -INFINITY;
+                p.lse[static_cast<size_t>(I.bh) * p.Sq + i] = lse;
+            }
+            release();
         }
     }
 
+    // Threads that issued TMA stores wait for their writes (not only for the
+    // shared-memory reads) before the CTA exits, so that the next kernel in the
+    // stream reads them.
+    tma_store_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     if (warp == kMmaWarp)
         tmem_dealloc(tmem, kTmemCols);
+    // The launch's last CTA to finish puts its work counters back to zero for
+    // the next launch that takes this slot.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.work + 1, 1ull) == gridDim.x - 1) {
+            atomicExch(p.work, 0ull);
+            atomicExch(p.work + 1, 0ull);
+        }
+    }
 }
 
 template <int D>
@@ -523,25 +677,52 @@ fa_status_t launch(const Problem &pr)
         !encode_tmap_bf16_3d(&tv, pr.v, D, pr.Sk, BH, kBlockN) ||
         !encode_tmap_bf16_3d(&to, pr.o, D, pr.Sq, BH, kBlockM))
         return FA_ERR_CUDA;
+    if (!pr.work_slots || pr.num_sms <= 0)
+        return FA_ERR_CUDA;
     Params p;
     p.Sq = static_cast<int>(pr.Sq);
     p.Sk = static_cast<int>(pr.Sk);
     p.BH = static_cast<int>(BH);
     p.n_qblk = static_cast<int>((pr.Sq + kTiles * kBlockM - 1) / (kTiles * kBlockM));
+    const uint64_t n_items = static_cast<uint64_t>(p.n_qblk) * BH;
+    if (n_items > 0x7FFFFFFFull)
+        return FA_ERR_UNSUPPORTED;
+    p.n_items = static_cast<int>(n_items);
+    // Item order. Causal items differ in cost (a query block's keys grow with
+    // its position), and when a CTA runs only a few of them the last ones
+    // decide the tail. Up to 2048 keys the heads are therefore taken in
+    // groups whose K/V share 48 MB of L2 and each group's query blocks go
+    // heaviest first across its heads; measured 0.87x / 0.88x the time of
+    // head-major order at S = 1024 / 2048. Longer causal problems and
+    // non-causal ones (equal items) keep head-major order (one head per
+    // group), which keeps each head's K/V reads together; grouping cost
+    // 1.02x at S = 4096.
+    p.heads_per_group = 1;
+    if (pr.causal && pr.Sk <= 2048) {
+        const double kv_head = 2.0 * static_cast<double>(pr.Sk) * D * 2.0;
+        const double budget = 48.0 * (1 << 20);
+        p.heads_per_group = static_cast<int>(
+            std::max(1.0, std::min(static_cast<double>(BH), std::floor(budget / kv_head))));
+    }
     p.causal = pr.causal ? 1 : 0;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.o = static_cast<__nv_bfloat16 *>(pr.o);
     p.lse = pr.lse;
     p.status = pr.status;
+    // Launches take the counter slots in turn; a slot is back at zero when its
+    // launch ends, so only launches more than kWorkSlots apart that run at the
+    // same time could share one.
+    static std::atomic<unsigned int> next_slot{0};
+    p.work = pr.work_slots + 2 * (next_slot.fetch_add(1, std::memory_order_relaxed) % kWorkSlots);
     auto kern = fa_prefill_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return FA_ERR_CUDA;
-
-    const uint64_t grid = static_cast<uint64_t>(p.n_qblk) * BH;
-    if (grid > 0x7FFFFFFFull)
-        return FA_ERR_UNSUPPORTED;
-    kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, pr.stream>>>(tq, tk, tv, to, p);
+    // Persistent: one CTA per SM (never more CTAs than items).
+    const unsigned grid =
+        static_cast<unsigned>(std::min<uint64_t>(n_items, static_cast<uint64_t>(pr.num_sms)));
+    kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -108,6 +108,11 @@ fa_status_t fa_forward_ws(const void *q, const void *k, const void *v, void *o, 
  * S = Q K^T with tcgen05 MMAs, applies the online softmax, accumulates
  * O += P V with tcgen05 MMAs, skips key tiles above the causal diagonal, and
  * writes O / l and LSE once. No workspace.
+ * The kernel is persistent (one CTA per SM) and takes its work items from a
+ * library-owned counter in device memory. Launches use the library's 1024
+ * counters in turn, and each launch returns its counter to zero, so up to
+ * 1024 launches may run at the same time; a 1025th running together with
+ * the one that took the same counter would share it.
  */
 fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void *o, float *lse,
                                int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,

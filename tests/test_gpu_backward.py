@@ -66,6 +66,25 @@ CASES = [
 ]
 
 
+def test_backward_rows_without_keys_after_cold_cache():
+    """Query tiles that see no key get dQ = 0. They load nothing: a Q load still
+    landing in the buffer that stages their zero tile would overwrite it. L2 is
+    flushed before each run so that such a load would be slow."""
+    B, H, Sq, Sk, d = 1, 2, 300, 100, 64
+    w = custom(B, H, Sq, Sk, d, True, seed=Sq + 3 * Sk, q_factor=2.0)
+    q, k, v = make_qkv(w)
+    do = upstream(q, w.seed)
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, True, w.scale)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(5):
+        flush.fill_(1)
+        dq, dk, dv = run_fwd_bwd(q, k, v, do, True, w.scale)
+        assert np.all(dq[:, :, :Sq - Sk] == 0.0)  # rows 0 .. Sq-Sk-1 see no key
+        check_grad("dq", dq, rq)
+        check_grad("dk", dk, rk)
+        check_grad("dv", dv, rv)
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}h{}q{}k{}d{}{}".format(*c[:5], "c" if c[5] else "n"))
 def test_backward_matches_oracle(case):
     B, H, Sq, Sk, d, causal = case
