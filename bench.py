@@ -94,6 +94,7 @@ def load_peaks():
         with open(path) as f:
             d = json.load(f)
         return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
                 "source": "measured"}
     return dict(FALLBACK_PEAKS, source="fallback")
 
@@ -206,22 +207,53 @@ def oracle_rows_flops(w, rows):
     return sum(4 * w.d * w.visible_keys(i) for _, _, i in rows)
 
 
-def time_oracle_sample(w, q, k, v, budget_s: float, seed: int = 7):
-    """Time the oracle (as it stands) on a seeded sample of rows sized to ~budget_s."""
+def time_oracle_sample(w, q, k, v, budget_s: float, seed: int = 7, threads: int = 0):
+    """Time the oracle (as it stands) on a seeded sample of rows sized to ~budget_s
+    (threads = 0: the OpenMP default)."""
     import oracle
 
     probe = sample_rows(w, n_total=16, seed=seed)
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.causal, w.scale, rows=probe)
+    oracle.attention(q, k, v, w.causal, w.scale, rows=probe, threads=threads)
     dt = max(time.perf_counter() - t0, 1e-6)
     per_flop = dt / oracle_rows_flops(w, probe)
     avg_row = w.exact_flops() / (w.B * w.H * w.Sq)
     n = int(max(16, min(w.B * w.H * w.Sq, budget_s / (per_flop * avg_row))))
     rows = sample_rows(w, n_total=n, seed=seed + 1)
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.causal, w.scale, rows=rows)
+    oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads)
     dt = time.perf_counter() - t0
     return rows, dt, oracle_rows_flops(w, rows)
+
+
+def measure_exp_pipe(w, device, sptr):
+    """The softmax's second bound: exp2 (MUFU) throughput from a microbenchmark,
+    against the exponentials one step of the prefill kernel computes (every
+    element of every computed tile; diagonal tiles are computed in full)."""
+    from exact_tiled_attention_03_gb300 import _capi
+
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    blocks, iters = sms * 8, 4096
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=device)
+    for _ in range(3):
+        _capi.check(_capi.fa_selftest_mufu(out, blocks, iters, sptr), "mufu")
+    stream = torch.cuda.current_stream(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
+        _capi.check(_capi.fa_selftest_mufu(out, blocks, iters, sptr), "mufu")
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    rate = 5 * blocks * 256 * iters * 8 / (a.elapsed_time(b) * 1e-3)
+    tiles = 0
+    n_q = -(-w.Sq // 128)
+    for qt in range(n_q):
+        last = min(qt * 128 + 127, w.Sq - 1)
+        tiles += -(-w.visible_keys(last) // 128)
+    exps = w.B * w.H * tiles * 128 * 128
+    return {"ex2_per_s": rate, "ex2_per_clk_per_sm_at_max_clock": rate / (sms * 2.07e9),
+            "exps_per_step": exps, "ms_lower_bound": exps / rate * 1e3,
+            "tensor_ms_lower_bound": w.exact_flops() / 1917.5e12 * 1e3}
 
 
 def run_reference(args, world, rank):
@@ -509,6 +541,9 @@ def run_ours(args, world, rank, local):
     if not args.no_fp8:
         fp8 = measure_fp8(w, device, sptr, args, peaks)
 
+    # the exp-pipe bound of the prefill step (MUFU microbenchmark)
+    exp_pipe = measure_exp_pipe(w, device, sptr)
+
     # the verify step's tree-mask and paged-cache forms, same bytes and roofline
     verify_ext = None
     if not args.no_verify:
@@ -520,11 +555,18 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
 
+        cores = oracle.max_threads()
         rows, dtc, flc = time_oracle_sample(w, q_h, k_h, v_h, budget_s=args.cpu_budget)
-        cpu = {"value": flc / dtc / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+        rows1, dt1, fl1 = time_oracle_sample(w, q_h, k_h, v_h, budget_s=2.0, seed=11, threads=1)
+        cpu = {"value": flc / dtc / 1e12, "unit": "TFLOP/s", "cores": cores,
                "kind": "oracle",
                "sample": f"{len(rows)} seeded query rows of {w.name} "
-                         f"({flc:.3e} algorithmic FLOPs, {dtc:.1f} s)"}
+                         f"({flc:.3e} algorithmic FLOPs, {dtc:.1f} s)",
+               "one_core_value": fl1 / dt1 / 1e12,
+               "one_core_sample": f"{len(rows1)} rows, {dt1:.1f} s",
+               "affinity_cpus": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None,
+               "omp_num_threads": os.environ.get("OMP_NUM_THREADS"),
+               "full_size_s_extrapolated": w.exact_flops() / (flc / dtc)}
 
     if rank == 0:
         line = {
@@ -535,12 +577,14 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "peak_source": f"{peaks['source']} bf16 burst",
+                         "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
+                         "peak_sustained": peaks["bf16_tflops_sustained"],
                          "kernel": "fa_prefill_kernel<128>",
                          "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, 1.0)},
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
             "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "backward": backward,
-            "fp8": fp8, "cpu_baseline": cpu,
+            "fp8": fp8, "exp_pipe": exp_pipe, "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": args.steps,  # one prefill kernel per timed step
             "gpu": torch.cuda.get_device_name(device),

@@ -51,6 +51,7 @@ SIGNATURES = {
     "fa_selftest_umma_ts": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_umma_f8": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_wait_timeout": (_I32, [_U64, _P]),
+    "fa_selftest_mufu": (_I32, [_P, _I32, _I32, _P]),
 }
 
 _lib = None
@@ -221,6 +222,10 @@ def fa_selftest_umma_ts(a, b, c, n, k, b_mn_major, stream=None) -> int:
 def fa_selftest_umma_f8(a, b, c, n, b_mn_major, a_tmem, stream=None) -> int:
     return load().fa_selftest_umma_f8(_ptr(a), _ptr(b), _ptr(c), int(n), int(b_mn_major),
                                       int(a_tmem), _stream(stream))
+
+
+def fa_selftest_mufu(out, blocks, iters, stream=None) -> int:
+    return load().fa_selftest_mufu(_ptr(out), int(blocks), int(iters), _stream(stream))
 
 
 def fa_selftest_wait_timeout(timeout_ns, stream=None) -> int:

@@ -738,6 +738,17 @@ fa_status_t fa_selftest_umma_f8(const void *a, const void *b, float *c, int n, i
                                    static_cast<cudaStream_t>(stream), di->status);
 }
 
+fa_status_t fa_selftest_mufu(float *out, int blocks, int iters, void *stream)
+{
+    if (!out || blocks <= 0 || iters <= 0)
+        return FA_ERR_INVALID_ARG;
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_mufu(out, blocks, iters, static_cast<cudaStream_t>(stream));
+}
+
 fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
 {
     if (timeout_ns == 0 || timeout_ns > 10000000000ull)

@@ -84,6 +84,7 @@ fa_status_t launch_selftest_umma(const void *a, const void *b, float *c, int n, 
 fa_status_t launch_selftest_umma_ts(const void *a, const void *b, float *c, int n, int k,
                                     int b_mn_major, cudaStream_t stream, unsigned int *status);
 fa_status_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t stream, unsigned int *status);
+fa_status_t launch_selftest_mufu(float *out, int blocks, int iters, cudaStream_t stream);
 
 // Split-KV geometry shared by the ABI (workspace sizing) and the launcher.
 constexpr int kVerifyStageKeys = 64;

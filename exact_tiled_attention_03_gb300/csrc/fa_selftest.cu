@@ -8,6 +8,7 @@
 //    (the operand form a P tile held in TMEM would use).
 //  * fa_selftest_umma_f8_kernel: the E4M3 products of the FP8 forward (A from
 //    shared or tensor memory, B K-major or MN-major).
+//  * fa_selftest_mufu_kernel: exp2 (MUFU) throughput, the softmax's second bound.
 //  * fa_selftest_wait_kernel: the bounded mbarrier wait of the attention
 //    kernels on a barrier that nothing completes; it must give up after the
 //    limit, set the device status word and return.
@@ -280,6 +281,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, 256);
 }
 
+// Throughput of the exp2 unit (MUFU) that the softmax uses: every thread runs
+// 8 independent chains of x <- ex2.approx(x) * c1 + c2 (the FMA keeps x in
+// range and costs a quarter of the FMA pipe's rate), so the kernel is bound by
+// ex2 issue. Each thread does iters * 8 ex2; the results are stored so that
+// nothing is removed by the compiler.
+__global__ void __launch_bounds__(256) fa_selftest_mufu_kernel(float *out, int iters)
+{
+    float x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        x[k] = -0.5f - 0.01f * static_cast<float>(k + (threadIdx.x & 7));
+    for (int n = 0; n < iters; ++n) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            x[k] = fmaf(ex2_approx(x[k]), -0.5f, -0.25f);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        s += x[k];
+    out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 __global__ void fa_selftest_wait_kernel(uint64_t limit_ns, unsigned int *status)
 {
     __shared__ uint64_t bar;
@@ -353,6 +377,12 @@ fa_status_t launch_selftest_umma_f8(const void *a, const void *b, float *c, int 
         return FA_ERR_CUDA;
     selftest::fa_selftest_umma_f8_kernel<<<1, selftest::kThreads, smem, stream>>>(
         ta, tb, static_cast<const float *>(a), c, n, b_mn_major, a_tmem, status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t launch_selftest_mufu(float *out, int blocks, int iters, cudaStream_t stream)
+{
+    selftest::fa_selftest_mufu_kernel<<<blocks, 256, 0, stream>>>(out, iters);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -60,6 +60,15 @@ fa_status_t fa_selftest_umma_f8(const void *a, const void *b, float *c, int n, i
                                 int a_tmem, void *stream);
 
 /*
+ * exp2 (MUFU) throughput microbenchmark: `blocks` CTAs of 256 threads, each
+ * thread running 8 independent chains of iters ex2.approx (with one FMA each to
+ * keep the values in range), i.e. blocks * 256 * iters * 8 ex2 in all. `out`
+ * receives one float per thread (blocks * 256, device memory). Time it with
+ * events on `stream`; it gives the softmax's exponential rate bound.
+ */
+fa_status_t fa_selftest_mufu(float *out, int blocks, int iters, void *stream);
+
+/*
  * Launches one CTA whose thread waits, with the same bounded wait the
  * attention kernels use, on an mbarrier that nothing ever completes. After
  * `timeout_ns` nanoseconds the wait gives up and sets the device status word

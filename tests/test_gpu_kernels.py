@@ -59,6 +59,18 @@ def test_tcgen05_a_operand_from_tensor_memory(n, k, b_mn_major):
     assert err < 1e-3 * math.sqrt(k), err
 
 
+def test_mufu_microbenchmark_runs():
+    """The exp2 throughput kernel the benchmark uses for the softmax's second bound."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = torch.full((sms * 256,), float("nan"), dtype=torch.float32, device="cuda")
+    _capi.check(_capi.fa_selftest_mufu(out, sms, 64), "mufu")
+    torch.cuda.synchronize()
+    v = out.cpu()
+    assert torch.isfinite(v).all()
+    # each chain settles at the fixed point of x = -0.5 * 2^x - 0.25 (about -0.59)
+    assert ((v / 8 + 0.59).abs() < 0.02).all()
+
+
 def test_bounded_wait_reports_a_timeout_without_faulting():
     """A wait on a barrier nothing completes gives up, sets the status word, returns."""
     assert _capi.fa_device_status() == _capi.FA_OK
