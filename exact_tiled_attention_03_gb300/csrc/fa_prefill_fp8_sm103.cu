@@ -18,18 +18,21 @@
 //   * a 128 x 128 E4M3 tile is one 128-byte-swizzled TMA box (16 KB), so
 //     the ring holds 8 tiles and Q two, in half the bytes of the bf16 kernel;
 //   * P is rounded to E4M3 before O += P V. The exponent is taken against an
-//     integer reference M in log2 units, P = 2^(x - M + 7) with
-//     x = s * scale * dq * dk * log2(e), so P <= 2^(7 + tau) stays inside
-//     E4M3's range (448) and every rescale factor 2^(M_old - M_new) is an
-//     exact power of two: rounding against M is rounding against the row's
-//     final reference up to that exact factor. M moves (to ceil of the tile
-//     max) only when a tile's max exceeds it by more than tau = 1.8, the
-//     largest tau with 2^(7 + tau) <= 448;
-//   * with so small a tau the reference moves often, so instead of the bf16
-//     kernel's speculative exponentials (redone when the max moves) each tile
-//     is read twice from TMEM: a max-only pass, then one exponential pass
-//     against the settled reference (measured 1.42 ms against 1.81 ms for
-//     the speculative form at B4 H32 S8192);
+//     integer reference M in log2 units, P = 2^(x - M + 4) with
+//     x = s * scale * dq * dk * log2(e). M moves (to ceil of the tile max)
+//     only when a tile's max exceeds it by more than tau = 4.8, so
+//     P <= 2^(4 + 4.8) stays inside E4M3's range (448), and every rescale
+//     factor 2^(M_old - M_new) is an exact power of two. As in the bf16
+//     kernel the exponentials are computed against the current reference
+//     while the tile's max is found, and redone only when the reference moves
+//     (rare with tau = 4.8: in practice only on a row's first tile);
+//   * relative to the row's final power-of-two max the effective scale of P
+//     is 2^4 to 2^9, so every weight of at least 2^-10 of the row max rounds
+//     to the same E4M3 value, up to an exact power of two, as with the scale
+//     2^7 the reference rounding uses; smaller weights may fall on E4M3's
+//     subnormal grid, a difference of at most 2^-13 of the row's largest
+//     weight each (measured: 1.31 ms here against 1.42 ms for a max-first
+//     form whose scale 2^7 allows tau <= 1.8 only);
 //   * P is packed four per 32-bit TMEM column (32 columns per 128 keys),
 //     the A operand of the P V product read from tensor memory;
 //   * the row sum l adds the fp32 P before rounding, so the LSE is that of
@@ -58,8 +61,8 @@ constexpr int kTileBytes = kBlockM * kD;   // one E4M3 tile = one TMA box (16 KB
 constexpr int kOutBoxBytes = kBlockM * 128;  // a 128-row x 64-column bf16 box
 constexpr int kOutTileBytes = kBlockM * kD * 2;
 constexpr int kStages = 8;
-constexpr int kPShift = 7;       // P = 2^(x - M + kPShift)
-constexpr float kTau = 1.8f;     // lazy-rescale threshold, log2 units: 2^(kPShift + kTau) <= 448
+constexpr int kPShift = 4;       // P = 2^(x - M + kPShift)
+constexpr float kTau = 4.8f;     // lazy-rescale threshold, log2 units: 2^(kPShift + kTau) <= 448
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kTiles * kTileBytes;
 constexpr int kOffOut = kOffKV + kStages * kTileBytes;
@@ -322,9 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key0 = j * kBlockN;
             uint32_t pk[kBlockN / 4];
             float2 acc[4];
-            // One pass over S_t: load and mask, then either find the raw max
-            // (with_exp false) or form P = 2^(s sl2 + neg), summed into acc and
-            // packed as E4M3 into pk (with_exp true).
+            // One pass over S_t: load, mask, and (with_exp) P = 2^(s sl2 + neg)
+            // summed into acc and packed as E4M3 into pk. Returns the raw max.
             auto pass = [&](bool with_exp, float neg) {
                 const float2 negx2 = make_float2(neg, neg);
                 float mx = -INFINITY;
@@ -345,20 +347,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (key0 + c0 + c >= lim)
                                 sv[c] = -INFINITY;
                     }
-                    if (!with_exp) {
-                        float part[kChunk / 16];
+                    float part[kChunk / 16];
 #pragma unroll
-                        for (int k = 0; k < kChunk / 16; ++k) {
-                            float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
+                    for (int k = 0; k < kChunk / 16; ++k) {
+                        float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
 #pragma unroll
-                            for (int e = 3; e < 15; e += 2)
-                                x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
-                            part[k] = fmaxf(x, sv[16 * k + 15]);
-                        }
+                        for (int e = 3; e < 15; e += 2)
+                            x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
+                        part[k] = fmaxf(x, sv[16 * k + 15]);
+                    }
 #pragma unroll
-                        for (int k = 0; k < kChunk / 16; ++k)
-                            mx = fmaxf(mx, part[k]);
-                    } else {
+                    for (int k = 0; k < kChunk / 16; ++k)
+                        mx = fmaxf(mx, part[k]);
+                    if (with_exp) {
 #pragma unroll
                         for (int c = 0; c < kChunk / 4; ++c) {
                             const float2 xa = ffma2(make_float2(sv[4 * c], sv[4 * c + 1]), sl2x2, negx2);
@@ -372,17 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return mx;
             };
-            const float mx = pass(false, 0.0f);
+            const bool spec = __all_sync(0xffffffffu, M != -INFINITY);
+            const float mx = pass(spec, spec ? static_cast<float>(kPShift) - M : 0.0f);
             // x_max > M + tau moves the reference to ceil(x_max); NaN-free since
             // M = -inf with x_max = -inf compares false.
             const float xm = mx * sl2;
             const bool move = xm > M + kTau;
             const float M_use = move ? ceilf(xm) : M;
             const float corr = move ? exp2_int(M - M_use) : 1.0f;  // exact; 0 when M = -inf
-            pass(true, (M_use == -INFINITY) ? 0.0f : static_cast<float>(kPShift) - M_use);
-            {
-                // O_t *= corr (warp-uniform; lanes that did not move multiply by
-                // 1). PV_t(j-1) has completed: S_t(j), committed after it, is done.
+            if (!spec || __any_sync(0xffffffffu, move)) {
+                pass(true, (M_use == -INFINITY) ? 0.0f : static_cast<float>(kPShift) - M_use);
                 if (j > 0 && __any_sync(0xffffffffu, move)) {
                     const float2 cx2 = make_float2(corr, corr);
 #pragma unroll

@@ -131,13 +131,17 @@ fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void
  *             one fp32 per tensor: a byte stands for descale * its E4M3 value.
  * It computes, per row, the scores s_j = scale * q_descale * k_descale *
  * (q . k_j) accumulated in fp32 on the FP8 tensor cores, the online softmax
- * with an integer reference M in log2 units, weights P_j = 2^(s_j log2 e - M)
- * rounded to E4M3 (nearest, ties to even) before O += P V runs on the FP8
- * tensor cores, the row sum l taken before that rounding, then
- * o = v_descale * O / l and lse = ln(sum_j e^(s_j)) (natural log; -inf and
- * o = 0 for a row with no visible key). Because M is an integer, the
- * rounded weights equal those rounded against the row's final max up to an
- * exact power of two. Causal masking is bottom-right as in fa_forward.
+ * with an integer reference M in log2 units, weights 2^(s_j log2 e - M)
+ * scaled by 2^4 and rounded to E4M3 (nearest, ties to even) before O += P V
+ * runs on the FP8 tensor cores, the row sum l taken before that rounding,
+ * then o = v_descale * O / l and lse = ln(sum_j e^(s_j)) (natural log; -inf
+ * and o = 0 for a row with no visible key). M is an integer that trails the
+ * row's running max by less than 4.8, so against the row's final max the
+ * weights are rounded at a scale of 2^4 to 2^9: every weight of at least
+ * 2^-10 of the row max gets the value the scale 2^7 gives (up to an exact
+ * power of two); smaller ones may round on E4M3's subnormal grid (at most
+ * 2^-13 of the row's largest weight each). Causal masking is bottom-right as
+ * in fa_forward.
  * d must be 128; q, k, v, o 16-byte aligned, lse 4-byte aligned; any
  * Sq, Sk >= 1. The caller owns every buffer; nothing is allocated.
  * Errors: FA_ERR_INVALID_ARG for null pointers, sizes <= 0, a non-finite

@@ -1,11 +1,13 @@
 """GPU parity of the FP8 forward (fa_forward_fp8), through the C ABI, against the
 oracle's FP8 path on the same seeded E4M3 inputs, element by element.
 
-The oracle rounds P to E4M3 against the row's power-of-two max exactly as the
-entry point's contract states; the kernel reaches the same weights up to an
-exact power of two, so the remaining differences are fp32 accumulation, the
-exp2 approximation (which can move a weight that sits within ~1e-7 of an
-E4M3 rounding tie to the neighbouring grid point) and the bf16 output. The bar
+The oracle rounds P to E4M3 at the scale 2^7 against the row's power-of-two
+max. The kernel's scale is 2^4 to 2^9 against its trailing reference, which
+gives the same weights (up to an exact power of two) for every weight of at
+least 2^-10 of the row max; smaller weights may round on E4M3's subnormal
+grid. The other differences are fp32 accumulation, the exp2 approximation
+(which can move a weight that sits within ~1e-7 of an E4M3 rounding tie to the
+neighbouring grid point) and the bf16 output. The bar
 is the one of the bf16 path: O max-abs 2e-2, mean-abs 2e-3, LSE 1e-3. One case
 also checks the kernel against the unrounded definition with the bound
 E4M3's three mantissa bits give.
