@@ -140,7 +140,7 @@ fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void
  * weights are rounded at a scale of 2^4 to 2^9: every weight of at least
  * 2^-10 of the row max gets the value the scale 2^7 gives (up to an exact
  * power of two); smaller ones may round on E4M3's subnormal grid (at most
- * 2^-13 of the row's largest weight each). Causal masking is bottom-right as
+ * 2^-12 of the row's largest weight each). Causal masking is bottom-right as
  * in fa_forward.
  * d must be 128; q, k, v, o 16-byte aligned, lse 4-byte aligned; any
  * Sq, Sk >= 1. The caller owns every buffer; nothing is allocated.
