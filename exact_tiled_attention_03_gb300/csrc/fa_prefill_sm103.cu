@@ -235,9 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_stream = l2_policy_evict_first();  // Q: read once
             const uint64_t pol_keep = l2_policy_evict_last();     // K/V: re-read by other q-blocks
             int it = 0;                       // ring index, continuous across items
-            uint32_t q_loads[kTiles] = {0, 0};  // q_full phases started
-            bool q_busy[kTiles] = {false, false};  // Q_t still read by the last item's MMAs
-            uint32_t o_phases[kTiles] = {0, 0};    // o_done phases of items with keys
+            // Q_t loads so far. Each is for an item with keys on tile t, which
+            // also completes one o_done[t] phase when its last MMA is done.
+            uint32_t q_loads[kTiles] = {0, 0};
             bool ok = true;
             auto load_kv = [&](int j, int which, int bh) {
                 const int s = it % C::kStages;
@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     // Q_t's buffer is free once the previous item's last MMA on
                     // tile t has completed.
-                    if (q_busy[t] &&
-                        !mbar_wait(&bars->o_done[t], (o_phases[t] - 1) & 1, abort_flag, p.status)) {
+                    if (q_loads[t] > 0 &&
+                        !mbar_wait(&bars->o_done[t], (q_loads[t] - 1) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -282,8 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d_hint(sQ + t * C::kTileBytes + b * kBoxBytes, &tm_q,
                                          &bars->q_full[t], b * 64, I.q0[t], I.bh, pol_stream);
                     ++q_loads[t];
-                    q_busy[t] = true;
-                    ++o_phases[t];
                 }
                 for (int j = 1; j < I.n_kv_max && ok; ++j)
                     ok = load_kv(j, 0, I.bh) && load_kv(j, 1, I.bh);
