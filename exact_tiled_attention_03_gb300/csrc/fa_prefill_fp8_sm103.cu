@@ -9,14 +9,17 @@
 // "Warmup Guide — Inference Optimization at Depth", Chapter 4 (online
 // softmax, causal tiles skipped or masked, O / l written once with the LSE).
 //
-// It keeps the bf16 kernel's structure (fa_prefill_sm103.cu): one CTA owns
-// two 128-row query tiles, warp 8 feeds a TMA ring of K/V tiles, warp 9
-// issues tcgen05.mma (here .kind::f8f6f4, 32 elements of K per instruction),
-// warps 0-3 and 4-7 run the softmax of one tile each with S and O in tensor
-// memory, and the MMA order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) overlaps
-// each tile's softmax with the other's products. What differs:
+// It keeps the bf16 kernel's structure (fa_prefill_sm103.cu): persistent CTAs
+// take work items (two 128-row query tiles of one head, fa_schedule.cuh) from
+// a per-launch counter and pass them to their warps through a shared-memory
+// queue; warp 8 feeds a TMA ring of K/V tiles, warp 9 issues tcgen05.mma
+// (here .kind::f8f6f4, 32 elements of K per instruction), warps 0-3 and 4-7
+// run the softmax of one tile each with S and O in tensor memory, and the MMA
+// order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) overlaps each tile's softmax
+// with the other's products. What differs:
 //   * a 128 x 128 E4M3 tile is one 128-byte-swizzled TMA box (16 KB), so
-//     the ring holds 8 tiles and Q two, in half the bytes of the bf16 kernel;
+//     the ring holds 8 tiles and Q two, and each tile has a whole 32 KB
+//     staging buffer for its bf16 O tile;
 //   * P is rounded to E4M3 before O += P V. The exponent is taken against an
 //     integer reference M in log2 units, P = 2^(x - M + 4) with
 //     x = s * scale * dq * dk * log2(e). M moves (to ceil of the tile max)
@@ -31,18 +34,18 @@
 //     to the same E4M3 value, up to an exact power of two, as with the scale
 //     2^7 the reference rounding uses; smaller weights may fall on E4M3's
 //     subnormal grid, a difference of at most 2^-12 of the row's largest
-//     weight each (measured: 1.31 ms here against 1.42 ms for a max-first
-//     form whose scale 2^7 allows tau <= 1.8 only);
+//     weight each (measured: 1.31 ms against 1.42 ms for a max-first form
+//     whose scale 2^7 allows tau <= 1.8 only);
 //   * P is packed four per 32-bit TMEM column (32 columns per 128 keys),
 //     the A operand of the P V product read from tensor memory;
 //   * the row sum l adds the fp32 P before rounding, so the LSE is that of
-//     the unrounded weights; O is scaled by v_descale / l and written as bf16
-//     through its own staging buffer.
+//     the unrounded weights; O is scaled by v_descale / l and written as bf16.
 // Every wait is bounded as in the bf16 kernel.
 #include <cmath>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_schedule.cuh"
 
 namespace fa {
 namespace prefill_fp8 {
@@ -50,7 +53,7 @@ namespace prefill_fp8 {
 constexpr int kD = 128;        // head dimension (bytes per E4M3 row)
 constexpr int kBlockM = 128;   // query rows per tile = TMEM lanes
 constexpr int kBlockN = 128;   // keys per K/V tile
-constexpr int kTiles = 2;      // query tiles per CTA
+constexpr int kTiles = 2;      // query tiles per item
 constexpr int kThreads = 320;  // 2 softmax warpgroups + producer warp + MMA warp
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
@@ -69,40 +72,43 @@ constexpr int kOffOut = kOffKV + kStages * kTileBytes;
 constexpr int kOffBar = kOffOut + kTiles * kOutTileBytes;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kTiles == sched::kTiles && kBlockM == sched::kTileRows && kBlockN == sched::kKeyTile,
+              "the kernel's tiles are the schedule's items");
 // S_t in TMEM columns [128 t, 128 t + 128); P_t (E4M3, four per column)
 // over its first 32 columns; O_t in [256 + 128 t, 256 + 128 t + 128).
 __device__ __forceinline__ uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * static_cast<uint32_t>(t); }
 
 struct Params {
-    int Sq, Sk, n_qblk;
-    int causal;
-    float sl2;      // scale * q_descale * k_descale * log2(e)
+    sched::Schedule sc;  // items and their order (fa_schedule.cuh)
+    float sl2;           // scale * q_descale * k_descale * log2(e)
     float v_descale;
     float *lse;
     unsigned int *status;
 };
 
+// Work-item queue slots, released when the consumers finish their item (at
+// most one item beyond the running one per CTA).
+constexpr int kQueue = 2;
+
 struct Bars {
-    uint64_t q_full;
-    uint64_t s_full[kTiles];
-    uint64_t p_full[kTiles];
-    uint64_t o_done[kTiles];
+    uint64_t q_full[kTiles];   // Q_t of the current item landed (one phase per item with keys)
+    uint64_t s_full[kTiles];   // S_t(j) in TMEM (one phase per key tile)
+    uint64_t p_full[kTiles];   // P_t(j) in TMEM and O_t rescaled (one phase per key tile)
+    uint64_t o_done[kTiles];   // last O_t += P_t V completed (one phase per item with keys)
+    uint64_t item_full[kQueue];
+    uint64_t item_empty[kQueue];
     uint64_t drain;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
+    int items[kQueue];
     uint32_t tmem_base;
     int abort_flag;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-__device__ __forceinline__ int visible_keys(int i, int Sq, int Sk, int causal)
-{
-    if (!causal)
-        return Sk;
-    int n = i + (Sk - Sq) + 1;
-    return n < 0 ? 0 : (n > Sk ? Sk : n);
-}
+using sched::Item;
+using sched::visible_keys;
 
 // 2^k for an integer k <= 0 given as a float (0 below the normal range or for -inf).
 __device__ __forceinline__ float exp2_int(float k)
@@ -127,31 +133,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int bh = static_cast<int>(blockIdx.x / p.n_qblk);
-    const int qblk = p.n_qblk - 1 - static_cast<int>(blockIdx.x % p.n_qblk);
-
-    int q0[kTiles], n_kv[kTiles], mask_from[kTiles];
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-        q0[t] = qblk * (kTiles * kBlockM) + t * kBlockM;
-        if (q0[t] < p.Sq) {
-            const int last = min(q0[t] + kBlockM - 1, p.Sq - 1);
-            n_kv[t] = (visible_keys(last, p.Sq, p.Sk, p.causal) + kBlockN - 1) / kBlockN;
-            mask_from[t] = visible_keys(q0[t], p.Sq, p.Sk, p.causal) / kBlockN;
-        } else {
-            n_kv[t] = 0;
-            mask_from[t] = 0;
-        }
-    }
-    const int n_kv_max = max(n_kv[0], n_kv[1]);
-    const bool any_tile = q0[0] < p.Sq;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 1);
         for (int t = 0; t < kTiles; ++t) {
+            mbar_init(&bars->q_full[t], 1);
             mbar_init(&bars->s_full[t], 1);
             mbar_init(&bars->p_full[t], 4);
             mbar_init(&bars->o_done[t], 1);
+        }
+        for (int s = 0; s < kQueue; ++s) {
+            mbar_init(&bars->item_full[s], 1);
+            mbar_init(&bars->item_empty[s], 1 + kSoftmaxWarps);  // MMA thread + softmax warps
         }
         mbar_init(&bars->drain, 1);
         for (int s = 0; s < kStages; ++s) {
@@ -179,43 +171,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && any_tile) {
-            const uint64_t pol_stream = l2_policy_evict_first();
-            const uint64_t pol_keep = l2_policy_evict_last();
-            uint32_t q_bytes = 0;
-            for (int t = 0; t < kTiles; ++t)
-                if (q0[t] < p.Sq)
-                    q_bytes += kTileBytes;
-            mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-            for (int t = 0; t < kTiles; ++t)
-                if (q0[t] < p.Sq)
-                    tma_load_3d_hint(sQ + t * kTileBytes, &tm_q, &bars->q_full, 0, q0[t], bh,
-                                     pol_stream);
-            int it = 0;
+        // Takes work items from the launch's counter, publishes each to the
+        // other roles through the item queue, then loads its Q tiles and its
+        // K_j, V_j through the ring, as the bf16 kernel does.
+        if (lane == 0) {
+            const uint64_t pol_stream = l2_policy_evict_first();  // Q: read once
+            const uint64_t pol_keep = l2_policy_evict_last();     // K/V: re-read by other q-blocks
+            int it = 0;                         // ring index, continuous across items
+            // Q_t loads so far. Each is for an item with keys on tile t, which
+            // also completes one o_done[t] phase when its last MMA is done.
+            uint32_t q_loads[kTiles] = {0, 0};
             bool ok = true;
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                for (int which = 0; which < 2 && ok; ++which, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t use = it / kStages;
-                    if (use > 0 &&
-                        !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status)) {
+            auto load_kv = [&](int j, int which, int bh) {
+                const int s = it % kStages;
+                const uint32_t use = it / kStages;
+                if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status))
+                    return false;
+                mbar_arrive_expect_tx(&bars->kv_full[s], kTileBytes);
+                tma_load_3d_hint(sKV + s * kTileBytes, which == 0 ? &tm_k : &tm_v,
+                                 &bars->kv_full[s], 0, j * kBlockN, bh, pol_keep);
+                ++it;
+                return true;
+            };
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kQueue;
+                if (n >= kQueue &&
+                    !mbar_wait(&bars->item_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status))
+                    break;
+                const int w = sched::grab_item(p.sc);
+                bars->items[slot] = w;
+                mbar_arrive(&bars->item_full[slot]);  // release: the consumers read items[slot]
+                if (w < 0)
+                    break;
+                const Item I = sched::decode_item(w, p.sc);
+                if (I.n_kv_max == 0)
+                    continue;
+                // K_0 and V_0 first: they do not wait for the Q buffers.
+                ok = load_kv(0, 0, I.bh) && load_kv(0, 1, I.bh);
+                for (int t = 0; t < kTiles && ok; ++t) {
+                    if (I.n_kv[t] == 0)
+                        continue;
+                    // Q_t's buffer is free once the previous item's last MMA on
+                    // tile t has completed.
+                    if (q_loads[t] > 0 &&
+                        !mbar_wait(&bars->o_done[t], (q_loads[t] - 1) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->kv_full[s], kTileBytes);
-                    tma_load_3d_hint(sKV + s * kTileBytes, which == 0 ? &tm_k : &tm_v,
-                                     &bars->kv_full[s], 0, j * kBlockN, bh, pol_keep);
+                    mbar_arrive_expect_tx(&bars->q_full[t], kTileBytes);
+                    tma_load_3d_hint(sQ + t * kTileBytes, &tm_q, &bars->q_full[t], 0, I.q0[t], I.bh,
+                                     pol_stream);
+                    ++q_loads[t];
                 }
+                for (int j = 1; j < I.n_kv_max && ok; ++j)
+                    ok = load_kv(j, 0, I.bh) && load_kv(j, 1, I.bh);
             }
-            mbar_wait_drain(&bars->q_full, 0, p.status);
+            // Drain: every load issued must have landed before the CTA exits.
+            for (int t = 0; t < kTiles; ++t)
+                if (q_loads[t] > 0)
+                    mbar_wait_drain(&bars->q_full[t], (q_loads[t] - 1) & 1, p.status);
             for (int k = max(0, it - kStages); k < it; ++k)
                 mbar_wait_drain(&bars->kv_full[k % kStages], (k / kStages) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Ring order K_0, V_0, K_1, V_1, ...; issue order S_0(0), S_1(0), then
-        // per j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), as in the bf16 kernel.
-        if (lane == 0 && any_tile && n_kv_max > 0) {
+        // Per item, ring order K_0, V_0, K_1, V_1, ...; issue order S_0(0),
+        // S_1(0), then per j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), as in the
+        // bf16 kernel.
+        if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_e4m3_f32(kBlockM, kBlockN, false, false);
             constexpr uint32_t idesc_pv = idesc_e4m3_f32(kBlockM, kD, false, true);
             const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
@@ -244,51 +267,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return mbar_wait(&bars->kv_full[idx % kStages], (idx / kStages) & 1, abort_flag,
                                  p.status);
             };
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status) && ring_wait(0);
-            if (ok) {
-                tc_fence_after_sync();
-                for (int t = 0; t < kTiles; ++t)
-                    if (n_kv[t] > 0) {
-                        issue_s(t, 0);
-                        umma_commit(&bars->s_full[t]);
-                    }
-                umma_commit(&bars->kv_empty[0]);
-            }
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                const int iv = 2 * j + 1, ik = 2 * j + 2;
-                ok = ring_wait(iv);
-                if (!ok)
+            int it = 0;
+            uint32_t q_waits[kTiles] = {0, 0}, p_waits[kTiles] = {0, 0};
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kQueue;
+                if (!mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status))
                     break;
-                tc_fence_after_sync();
-                bool k_ready = false;
+                const int w = bars->items[slot];
+                if (w < 0)
+                    break;
+                const Item I = sched::decode_item(w, p.sc);
+                if (I.n_kv_max == 0) {
+                    mbar_arrive(&bars->item_empty[slot]);
+                    continue;
+                }
+                // S_t(0) as soon as Q_t is in.
+                ok = ring_wait(it);  // K_0
                 for (int t = 0; t < kTiles && ok; ++t) {
-                    if (j >= n_kv[t])
+                    if (I.n_kv[t] == 0)
                         continue;
-                    ok = mbar_wait(&bars->p_full[t], j & 1, abort_flag, p.status);
+                    ok = mbar_wait(&bars->q_full[t], (q_waits[t]++) & 1, abort_flag, p.status);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
-                    issue_pv(t, iv % kStages, j);
-                    if (j + 1 < n_kv[t]) {
-                        if (!k_ready) {
-                            ok = ring_wait(ik);
-                            if (!ok)
-                                break;
-                            tc_fence_after_sync();
-                            k_ready = true;
-                        }
-                        issue_s(t, ik % kStages);
-                        umma_commit(&bars->s_full[t]);
-                    } else {
-                        umma_commit(&bars->o_done[t]);
-                    }
+                    issue_s(t, it % kStages);
+                    umma_commit(&bars->s_full[t]);
                 }
                 if (!ok)
                     break;
-                umma_commit(&bars->kv_empty[iv % kStages]);
-                if (k_ready)
-                    umma_commit(&bars->kv_empty[ik % kStages]);
+                umma_commit(&bars->kv_empty[it % kStages]);
+                for (int j = 0; j < I.n_kv_max && ok; ++j) {
+                    const int iv = it + 2 * j + 1, ik = it + 2 * j + 2;
+                    ok = ring_wait(iv);  // V_j
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    bool k_ready = false;
+                    for (int t = 0; t < kTiles && ok; ++t) {
+                        if (j >= I.n_kv[t])
+                            continue;
+                        ok = mbar_wait(&bars->p_full[t], (p_waits[t]++) & 1, abort_flag, p.status);
+                        if (!ok)
+                            break;
+                        tc_fence_after_sync();
+                        issue_pv(t, iv % kStages, j);
+                        if (j + 1 < I.n_kv[t]) {
+                            if (!k_ready) {
+                                ok = ring_wait(ik);  // K_{j+1}
+                                if (!ok)
+                                    break;
+                                tc_fence_after_sync();
+                                k_ready = true;
+                            }
+                            issue_s(t, ik % kStages);
+                            umma_commit(&bars->s_full[t]);
+                        } else {
+                            umma_commit(&bars->o_done[t]);  // this tile's last PV of the item
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    umma_commit(&bars->kv_empty[iv % kStages]);
+                    if (k_ready)
+                        umma_commit(&bars->kv_empty[ik % kStages]);
+                }
+                it += 2 * I.n_kv_max;
+                mbar_arrive(&bars->item_empty[slot]);  // every MMA of the item is issued
             }
+            // Drain: all MMAs issued by this thread complete before TMEM is freed.
             umma_commit(&bars->drain);
             mbar_wait_drain(&bars->drain, 0, p.status);
         }
@@ -297,172 +344,212 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp / 4;
         const int wq = warp % 4;
         const int r = wq * 32 + lane;
-        const int i = q0[t] + r;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_base + col_s(t);
         const uint32_t tO = tmem + lane_base + col_o(t);
         uint8_t *sOut = smem + kOffOut + t * kOutTileBytes;
         const uint32_t sOut_a = smem_u32(sOut);
-        const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
         const float sl2 = p.sl2;
-
-        // M: the integer reference (log2 units) of this row's exponentials,
-        // -inf until a key is visible. O and l always share it.
-        float M = -INFINITY;
-        float l = 0.0f;
-        bool ok = true;
-        if (q0[t] < p.Sq)
-            ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-
         const float2 sl2x2 = make_float2(sl2, sl2);
-        for (int j = 0; j < n_kv[t] && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort_flag, p.status));
-            if (!ok)
+        uint32_t s_waits = 0, o_waits = 0;  // phases of s_full[t] and o_done[t] consumed
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            const int slot = n % kQueue;
+            // Waits feed .sync.aligned TMEM instructions: keep their outcome
+            // warp-uniform. The tile's 4 warps also leave the loop together
+            // (their epilogue has named barriers), so the outcome is made
+            // tile-uniform here.
+            const bool got_item = __all_sync(
+                0xffffffffu,
+                mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status));
+            if (named_bar_or(1 + t, 128, !got_item))
                 break;
-            tc_fence_after_sync();
-            const bool masked_tile = j >= mask_from[t];
-            const int key0 = j * kBlockN;
-            uint32_t pk[kBlockN / 4];
-            float2 acc[4];
-            // One pass over S_t: load, mask, and (with_exp) P = 2^(s sl2 + neg)
-            // summed into acc and packed as E4M3 into pk. Returns the raw max.
-            auto pass = [&](bool with_exp, float neg) {
-                const float2 negx2 = make_float2(neg, neg);
-                float mx = -INFINITY;
+            const int w = *reinterpret_cast<volatile int *>(&bars->items[slot]);
+            if (w < 0)
+                break;
+            // The item's slot is released when this warp has finished the item.
+            auto release = [&]() {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->item_empty[slot]);
+            };
+            const Item I = sched::decode_item(w, p.sc);
+            const int q0 = I.q0[t], n_kv = I.n_kv[t], mask_from = I.mask_from[t];
+            const int i = q0 + r;  // query row
+            const int lim = visible_keys(i, p.sc.Sq, p.sc.Sk, p.sc.causal);
+
+            // M: the integer reference (log2 units) of this row's exponentials,
+            // -inf until a key is visible. O and l always share it.
+            float M = -INFINITY;
+            float l = 0.0f;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], (s_waits++) & 1,
+                                                       abort_flag, p.status));
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                const bool masked_tile = j >= mask_from;
+                const int key0 = j * kBlockN;
+                uint32_t pk[kBlockN / 4];
+                float2 acc[4];
+                // One pass over S_t: load, mask, and (with_exp) P = 2^(s sl2 + neg)
+                // summed into acc and packed as E4M3 into pk. Returns the raw max.
+                auto pass = [&](bool with_exp, float neg) {
+                    const float2 negx2 = make_float2(neg, neg);
+                    float mx = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    acc[q] = make_float2(0.f, 0.f);
+                    for (int q = 0; q < 4; ++q)
+                        acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int c0 = 0; c0 < kBlockN; c0 += kChunk) {
-                    uint32_t raw[kChunk];
-                    tmem_ld64_wait(tS + c0, raw);
-                    float sv[kChunk];
-#pragma unroll
-                    for (int c = 0; c < kChunk; ++c)
-                        sv[c] = __uint_as_float(raw[c]);
-                    if (masked_tile) {
+                    for (int c0 = 0; c0 < kBlockN; c0 += kChunk) {
+                        uint32_t raw[kChunk];
+                        tmem_ld64_wait(tS + c0, raw);
+                        float sv[kChunk];
 #pragma unroll
                         for (int c = 0; c < kChunk; ++c)
-                            if (key0 + c0 + c >= lim)
-                                sv[c] = -INFINITY;
+                            sv[c] = __uint_as_float(raw[c]);
+                        if (masked_tile) {
+#pragma unroll
+                            for (int c = 0; c < kChunk; ++c)
+                                if (key0 + c0 + c >= lim)
+                                    sv[c] = -INFINITY;
+                        }
+                        float part[kChunk / 16];
+#pragma unroll
+                        for (int k = 0; k < kChunk / 16; ++k) {
+                            float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
+#pragma unroll
+                            for (int e = 3; e < 15; e += 2)
+                                x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
+                            part[k] = fmaxf(x, sv[16 * k + 15]);
+                        }
+#pragma unroll
+                        for (int k = 0; k < kChunk / 16; ++k)
+                            mx = fmaxf(mx, part[k]);
+                        if (with_exp) {
+#pragma unroll
+                            for (int c = 0; c < kChunk / 4; ++c) {
+                                const float2 xa =
+                                    ffma2(make_float2(sv[4 * c], sv[4 * c + 1]), sl2x2, negx2);
+                                const float2 xb =
+                                    ffma2(make_float2(sv[4 * c + 2], sv[4 * c + 3]), sl2x2, negx2);
+                                const float2 ea = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+                                const float2 eb = make_float2(ex2_approx(xb.x), ex2_approx(xb.y));
+                                acc[c % 4] = fadd2(acc[c % 4], fadd2(ea, eb));
+                                pk[c0 / 4 + c] = pack_e4m3x4(ea.x, ea.y, eb.x, eb.y);
+                            }
+                        }
                     }
-                    float part[kChunk / 16];
+                    return mx;
+                };
+                const bool spec = __all_sync(0xffffffffu, M != -INFINITY);
+                const float mx = pass(spec, spec ? static_cast<float>(kPShift) - M : 0.0f);
+                // x_max > M + tau moves the reference to ceil(x_max); NaN-free
+                // since M = -inf with x_max = -inf compares false.
+                const float xm = mx * sl2;
+                const bool move = xm > M + kTau;
+                const float M_use = move ? ceilf(xm) : M;
+                const float corr = move ? exp2_int(M - M_use) : 1.0f;  // exact; 0 when M = -inf
+                if (!spec || __any_sync(0xffffffffu, move)) {
+                    pass(true, (M_use == -INFINITY) ? 0.0f : static_cast<float>(kPShift) - M_use);
+                    // O_t *= corr (warp-uniform; lanes that did not move multiply
+                    // by 1). PV_t(j-1) has completed: S_t(j), committed after it,
+                    // is done.
+                    if (j > 0 && __any_sync(0xffffffffu, move)) {
+                        const float2 cx2 = make_float2(corr, corr);
 #pragma unroll
-                    for (int k = 0; k < kChunk / 16; ++k) {
-                        float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
+                        for (int c0 = 0; c0 < kD; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32_wait(tO + c0, o);
 #pragma unroll
-                        for (int e = 3; e < 15; e += 2)
-                            x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
-                        part[k] = fmaxf(x, sv[16 * k + 15]);
-                    }
-#pragma unroll
-                    for (int k = 0; k < kChunk / 16; ++k)
-                        mx = fmaxf(mx, part[k]);
-                    if (with_exp) {
-#pragma unroll
-                        for (int c = 0; c < kChunk / 4; ++c) {
-                            const float2 xa = ffma2(make_float2(sv[4 * c], sv[4 * c + 1]), sl2x2, negx2);
-                            const float2 xb = ffma2(make_float2(sv[4 * c + 2], sv[4 * c + 3]), sl2x2, negx2);
-                            const float2 ea = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
-                            const float2 eb = make_float2(ex2_approx(xb.x), ex2_approx(xb.y));
-                            acc[c % 4] = fadd2(acc[c % 4], fadd2(ea, eb));
-                            pk[c0 / 4 + c] = pack_e4m3x4(ea.x, ea.y, eb.x, eb.y);
+                            for (int c = 0; c < 16; ++c) {
+                                const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
+                                                                   __uint_as_float(o[2 * c + 1])),
+                                                       cx2);
+                                o[2 * c] = __float_as_uint(v.x);
+                                o[2 * c + 1] = __float_as_uint(v.y);
+                            }
+                            tmem_st32(tO + c0, o);
                         }
                     }
                 }
-                return mx;
-            };
-            const bool spec = __all_sync(0xffffffffu, M != -INFINITY);
-            const float mx = pass(spec, spec ? static_cast<float>(kPShift) - M : 0.0f);
-            // x_max > M + tau moves the reference to ceil(x_max); NaN-free since
-            // M = -inf with x_max = -inf compares false.
-            const float xm = mx * sl2;
-            const bool move = xm > M + kTau;
-            const float M_use = move ? ceilf(xm) : M;
-            const float corr = move ? exp2_int(M - M_use) : 1.0f;  // exact; 0 when M = -inf
-            if (!spec || __any_sync(0xffffffffu, move)) {
-                pass(true, (M_use == -INFINITY) ? 0.0f : static_cast<float>(kPShift) - M_use);
-                if (j > 0 && __any_sync(0xffffffffu, move)) {
-                    const float2 cx2 = make_float2(corr, corr);
-#pragma unroll
-                    for (int c0 = 0; c0 < kD; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32_wait(tO + c0, o);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
-                                                               __uint_as_float(o[2 * c + 1])),
-                                                   cx2);
-                            o[2 * c] = __float_as_uint(v.x);
-                            o[2 * c + 1] = __float_as_uint(v.y);
-                        }
-                        tmem_st32(tO + c0, o);
-                    }
-                }
+                tmem_st32(tS, pk);  // P (E4M3, four per column) over S_t's first 32 columns
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->p_full[t]);
+                const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+                const float2 a = fadd2(a01, a23);
+                l = l * corr + (a.x + a.y);
+                M = M_use;
             }
-            tmem_st32(tS, pk);  // P (E4M3, four per column) over S_t's first 32 columns
-            tmem_st_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars->p_full[t]);
-            const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
-            const float2 a = fadd2(a01, a23);
-            l = l * corr + (a.x + a.y);
-            M = M_use;
-        }
 
-        // ------------------------------------------------------------ epilogue
-        if (ok && q0[t] < p.Sq) {
-            if (n_kv[t] > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], 0, abort_flag, p.status));
-                tc_fence_after_sync();
+            // -------------------------------------------------------- epilogue
+            // O * v_descale / l into this tile's staging buffer (swizzled like
+            // the TMA boxes), two TMA stores, then the LSE. The next item's P_t
+            // is published only after these TMEM reads, so its PV_t(0) cannot
+            // overwrite O_t early.
+            if (q0 >= p.sc.Sq) {
+                release();
+                continue;
             }
-            if (ok) {
-                const float mul = (l > 0.0f) ? p.v_descale / l : 0.0f;
+            bool got = ok;
+            if (got && n_kv > 0) {
+                got = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (o_waits++) & 1,
+                                                        abort_flag, p.status));
+                if (got)
+                    tc_fence_after_sync();
+            }
+            // The tile's 4 warps take the barriers below together or not at all.
+            if (named_bar_or(1 + t, 128, !got)) {
+                ok = false;
+                break;
+            }
+            const float mul = (l > 0.0f) ? p.v_descale / l : 0.0f;
 #pragma unroll
-                for (int c0 = 0; c0 < kD; c0 += 32) {
-                    uint32_t o[32];
-                    if (n_kv[t] > 0) {
-                        tmem_ld32_wait(tO + c0, o);
-                    } else {
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                uint32_t o[32];
+                if (n_kv > 0) {
+                    tmem_ld32_wait(tO + c0, o);
+                } else {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            o[c] = 0u;
-                    }
-                    uint32_t pkd[16];
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2)
-                        pkd[c / 2] = pack_bf16x2(__uint_as_float(o[c]) * mul,
-                                                 __uint_as_float(o[c + 1]) * mul);
-                    const int box = c0 / 64;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t chunk = ((c0 % 64) / 8) + q;
-                        st_shared_v4(sOut_a + box * kOutBoxBytes +
-                                         sw128_offset(static_cast<uint32_t>(r), chunk),
-                                     pkd[q * 4], pkd[q * 4 + 1], pkd[q * 4 + 2], pkd[q * 4 + 3]);
-                    }
+                    for (int c = 0; c < 32; ++c)
+                        o[c] = 0u;
                 }
-                if (i < p.Sq) {
-                    // lse = ln 2 * (M - kPShift + log2 l), in units of the scaled scores
-                    const float lse = (l > 0.0f)
-                                          ? (M - static_cast<float>(kPShift)) * 0.69314718055994531f +
-                                                logf(l)
-                                          : -INFINITY;
-                    p.lse[static_cast<size_t>(bh) * p.Sq + i] = lse;
+                uint32_t pkd[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2)
+                    pkd[c / 2] = pack_bf16x2(__uint_as_float(o[c]) * mul,
+                                             __uint_as_float(o[c + 1]) * mul);
+                const int box = c0 / 64;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t chunk = ((c0 % 64) / 8) + q;
+                    st_shared_v4(sOut_a + box * kOutBoxBytes +
+                                     sw128_offset(static_cast<uint32_t>(r), chunk),
+                                 pkd[q * 4], pkd[q * 4 + 1], pkd[q * 4 + 2], pkd[q * 4 + 3]);
                 }
             }
-        }
-        tc_fence_before_sync();
-        fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
-        if (r == 0 && ok && q0[t] < p.Sq && !*reinterpret_cast<volatile int *>(abort_flag)) {
-            for (int b = 0; b < kD / 64; ++b)
-                tma_store_3d(&tm_o, sOut + b * kOutBoxBytes, b * 64, q0[t], bh);
-            tma_store_commit();
-            tma_store_wait_read_all();
+            fence_proxy_async_smem();
+            named_bar_sync(1 + t, 128);
+            if (r == 0) {
+                for (int b = 0; b < kD / 64; ++b)
+                    tma_store_3d(&tm_o, sOut + b * kOutBoxBytes, b * 64, q0, I.bh);
+                tma_store_commit();
+                // The buffer is rewritten only after the tile's next barrier;
+                // the writes finish on their own.
+                tma_store_wait_read_all();
+            }
+            if (i < p.sc.Sq) {
+                // lse = ln 2 * (M - kPShift + log2 l), in units of the scaled scores
+                const float lse = (l > 0.0f)
+                                      ? (M - static_cast<float>(kPShift)) * 0.69314718055994531f +
+                                            logf(l)
+                                      : -INFINITY;
+                p.lse[static_cast<size_t>(I.bh) * p.sc.Sq + i] = lse;
+            }
+            release();
         }
     }
 
@@ -475,6 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     if (warp == kMmaWarp)
         tmem_dealloc(tmem, kTmemCols);
+    if (threadIdx.x == 0)
+        sched::finish_cta(p.sc);
 }
 
 }  // namespace prefill_fp8
@@ -493,25 +582,23 @@ fa_status_t launch_prefill_fp8_sm103(const Problem &pr, float q_descale, float k
         !encode_tmap_bf16_3d(&to, pr.o, kD, pr.Sq, BH, kBlockM))
         return FA_ERR_CUDA;
     Params p;
-    p.Sq = static_cast<int>(pr.Sq);
-    p.Sk = static_cast<int>(pr.Sk);
-    p.n_qblk = static_cast<int>((pr.Sq + kTiles * kBlockM - 1) / (kTiles * kBlockM));
-    p.causal = pr.causal ? 1 : 0;
     p.sl2 = static_cast<float>(static_cast<double>(pr.scale) * q_descale * k_descale *
                                1.4426950408889634);
+    if (!(p.sl2 > 0.0f) || !std::isfinite(p.sl2))
+        return FA_ERR_UNSUPPORTED;
+    unsigned grid = 0;
+    const fa_status_t st =
+        sched::make_schedule(pr, 2.0 * static_cast<double>(pr.Sk) * kD, &p.sc, &grid);
+    if (st != FA_OK)
+        return st;
     p.v_descale = v_descale;
     p.lse = pr.lse;
     p.status = pr.status;
-    if (!(p.sl2 > 0.0f) || !std::isfinite(p.sl2))
-        return FA_ERR_UNSUPPORTED;
     auto kern = fa_prefill_fp8_kernel;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return FA_ERR_CUDA;
-    const uint64_t grid = static_cast<uint64_t>(p.n_qblk) * BH;
-    if (grid > 0x7FFFFFFFull)
-        return FA_ERR_UNSUPPORTED;
-    kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, pr.stream>>>(tq, tk, tv, to, p);
+    kern<<<grid, kThreads, kSmemBytes, pr.stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -39,12 +39,11 @@
 //     the next item as soon as the item's MMAs are done.
 // Every wait is bounded; on expiry the CTA stops, drains what it has in
 // flight, frees its tensor memory and sets the device status word.
-#include <algorithm>
-#include <atomic>
 #include <cmath>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_schedule.cuh"
 
 namespace fa {
 namespace prefill {
@@ -89,14 +88,11 @@ struct Cfg {
 };
 
 struct Params {
-    int Sq, Sk, BH, n_qblk, n_items, heads_per_group;
-    int causal;
-    float scale;       // softmax scale
-    float scale_log2;  // scale * log2(e)
-    __nv_bfloat16 *o;
+    sched::Schedule sc;  // items and their order (fa_schedule.cuh)
+    float scale;         // softmax scale
+    float scale_log2;    // scale * log2(e)
     float *lse;
     unsigned int *status;
-    unsigned long long *work;  // this launch's (next item, finished CTAs) pair
 };
 
 // Work-item queue slots. The consumers release a slot when they have finished
@@ -120,56 +116,10 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-// Number of keys visible to query row i (bottom-right causal alignment).
-__device__ __forceinline__ int visible_keys(int i, int Sq, int Sk, int causal)
-{
-    if (!causal)
-        return Sk;
-    int n = i + (Sk - Sq) + 1;
-    return n < 0 ? 0 : (n > Sk ? Sk : n);
-}
-
-// Work item w: two query tiles of one (batch, head). Heads are taken in
-// groups of heads_per_group (the last group may be smaller); within a group
-// the query blocks go heaviest first (last block, most keys under the causal
-// mask), across all the group's heads. One head per group is head-major
-// order: items handed out together share a few heads' K/V in L2.
-struct Item {
-    int bh;
-    int q0[kTiles], n_kv[kTiles], mask_from[kTiles];
-    int n_kv_max;
-};
-
-__device__ __forceinline__ Item decode_item(int w, const Params &p)
-{
-    Item it;
-    const int per_group = p.heads_per_group * p.n_qblk;
-    const int g = w / per_group, rg = w % per_group;
-    const int hg = min(p.heads_per_group, p.BH - g * p.heads_per_group);
-    it.bh = g * p.heads_per_group + rg % hg;
-    const int qblk = p.n_qblk - 1 - rg / hg;
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-        it.q0[t] = qblk * (kTiles * kBlockM) + t * kBlockM;
-        if (it.q0[t] < p.Sq) {
-            const int last = min(it.q0[t] + kBlockM - 1, p.Sq - 1);
-            it.n_kv[t] = (visible_keys(last, p.Sq, p.Sk, p.causal) + kBlockN - 1) / kBlockN;
-            it.mask_from[t] = visible_keys(it.q0[t], p.Sq, p.Sk, p.causal) / kBlockN;
-        } else {
-            it.n_kv[t] = 0;
-            it.mask_from[t] = 0;
-        }
-    }
-    it.n_kv_max = max(it.n_kv[0], it.n_kv[1]);
-    return it;
-}
-
-// The next work item of this launch, or -1 when none is left.
-__device__ __forceinline__ int grab_item(const Params &p)
-{
-    const unsigned long long w = atomicAdd(p.work, 1ull);
-    return w < static_cast<unsigned long long>(p.n_items) ? static_cast<int>(w) : -1;
-}
+using sched::Item;
+using sched::visible_keys;
+static_assert(kTiles == sched::kTiles && kBlockM == sched::kTileRows && kBlockN == sched::kKeyTile,
+              "the kernel's tiles are the schedule's items");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -257,12 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n >= kQueue &&
                     !mbar_wait(&bars->item_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status))
                     break;
-                const int w = grab_item(p);
+                const int w = sched::grab_item(p.sc);
                 bars->items[slot] = w;
                 mbar_arrive(&bars->item_full[slot]);  // release: the consumers read items[slot]
                 if (w < 0)
                     break;
-                const Item I = decode_item(w, p);
+                const Item I = sched::decode_item(w, p.sc);
                 if (I.n_kv_max == 0)
                     continue;
                 // K_0 and V_0 first: they do not wait for the Q buffers.
@@ -345,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int w = bars->items[slot];
                 if (w < 0)
                     break;
-                const Item I = decode_item(w, p);
+                const Item I = sched::decode_item(w, p.sc);
                 if (I.n_kv_max == 0) {
                     mbar_arrive(&bars->item_empty[slot]);
                     continue;
@@ -440,10 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0)
                     mbar_arrive(&bars->item_empty[slot]);
             };
-            const Item I = decode_item(w, p);
+            const Item I = sched::decode_item(w, p.sc);
             const int q0 = I.q0[t], n_kv = I.n_kv[t], mask_from = I.mask_from[t];
             const int i = q0 + r;  // query row
-            const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
+            const int lim = visible_keys(i, p.sc.Sq, p.sc.Sk, p.sc.causal);
 
             // m: the reference max of this row's exponentials (raw score units,
             // scale > 0). It is updated lazily: only when a tile's max exceeds it
@@ -580,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 64-column box at a time, each sent by a TMA store, then the LSE.
             // The next item's P_t is published only after these TMEM reads, so
             // its PV_t(0) cannot overwrite O_t early.
-            if (q0 >= p.Sq) {
+            if (q0 >= p.sc.Sq) {
                 release();
                 continue;
             }
@@ -636,9 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_store_wait_read_all();
                 }
             }
-            if (i < p.Sq) {
+            if (i < p.sc.Sq) {
                 const float lse = (l > 0.0f) ? m * p.scale + logf(l) : -INFINITY;
-                p.lse[static_cast<size_t>(I.bh) * p.Sq + i] = lse;
+                p.lse[static_cast<size_t>(I.bh) * p.sc.Sq + i] = lse;
             }
             release();
         }
@@ -655,13 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     // The launch's last CTA to finish puts its work counters back to zero for
     // the next launch that takes this slot.
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(p.work + 1, 1ull) == gridDim.x - 1) {
-            atomicExch(p.work, 0ull);
-            atomicExch(p.work + 1, 0ull);
-        }
-    }
+    if (threadIdx.x == 0)
+        sched::finish_cta(p.sc);
 }
 
 template <int D>
@@ -675,51 +620,20 @@ fa_status_t launch(const Problem &pr)
         !encode_tmap_bf16_3d(&tv, pr.v, D, pr.Sk, BH, kBlockN) ||
         !encode_tmap_bf16_3d(&to, pr.o, D, pr.Sq, BH, kBlockM))
         return FA_ERR_CUDA;
-    if (!pr.work_slots || pr.num_sms <= 0)
-        return FA_ERR_CUDA;
     Params p;
-    p.Sq = static_cast<int>(pr.Sq);
-    p.Sk = static_cast<int>(pr.Sk);
-    p.BH = static_cast<int>(BH);
-    p.n_qblk = static_cast<int>((pr.Sq + kTiles * kBlockM - 1) / (kTiles * kBlockM));
-    const uint64_t n_items = static_cast<uint64_t>(p.n_qblk) * BH;
-    if (n_items > 0x7FFFFFFFull)
-        return FA_ERR_UNSUPPORTED;
-    p.n_items = static_cast<int>(n_items);
-    // Item order. Causal items differ in cost (a query block's keys grow with
-    // its position), and when a CTA runs only a few of them the last ones
-    // decide the tail. Up to 2048 keys the heads are therefore taken in
-    // groups whose K/V share 48 MB of L2 and each group's query blocks go
-    // heaviest first across its heads; measured 0.87x / 0.88x the time of
-    // head-major order at S = 1024 / 2048. Longer causal problems and
-    // non-causal ones (equal items) keep head-major order (one head per
-    // group), which keeps each head's K/V reads together; grouping cost
-    // 1.02x at S = 4096.
-    p.heads_per_group = 1;
-    if (pr.causal && pr.Sk <= 2048) {
-        const double kv_head = 2.0 * static_cast<double>(pr.Sk) * D * 2.0;
-        const double budget = 48.0 * (1 << 20);
-        p.heads_per_group = static_cast<int>(
-            std::max(1.0, std::min(static_cast<double>(BH), std::floor(budget / kv_head))));
-    }
-    p.causal = pr.causal ? 1 : 0;
+    unsigned grid = 0;
+    const fa_status_t st = sched::make_schedule(pr, 2.0 * static_cast<double>(pr.Sk) * D * 2.0,
+                                                &p.sc, &grid);
+    if (st != FA_OK)
+        return st;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
-    p.o = static_cast<__nv_bfloat16 *>(pr.o);
     p.lse = pr.lse;
     p.status = pr.status;
-    // Launches take the counter slots in turn; a slot is back at zero when its
-    // launch ends, so only launches more than kWorkSlots apart that run at the
-    // same time could share one.
-    static std::atomic<unsigned int> next_slot{0};
-    p.work = pr.work_slots + 2 * (next_slot.fetch_add(1, std::memory_order_relaxed) % kWorkSlots);
     auto kern = fa_prefill_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return FA_ERR_CUDA;
-    // Persistent: one CTA per SM (never more CTAs than items).
-    const unsigned grid =
-        static_cast<unsigned>(std::min<uint64_t>(n_items, static_cast<uint64_t>(pr.num_sms)));
     kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
