@@ -108,11 +108,13 @@ def source_hash(files):
 
 
 PREFILL_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_prefill_sm103.cu",
-                   "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
+                   "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh",
+                   "exact_tiled_attention_03_gb300/csrc/fa_schedule.cuh"]
 VERIFY_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_verify.cu",
                   "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
 FP8_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_prefill_fp8_sm103.cu",
-               "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
+               "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh",
+               "exact_tiled_attention_03_gb300/csrc/fa_schedule.cuh"]
 BWD_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_backward_sm103.cu",
                "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
 
