@@ -8,27 +8,36 @@
 //     dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
 //     dK = scale * dS^T Q,  dQ = scale * dS K.
 // Three kernels:
-//   * fa_bwd_prep_kernel: D_i and LSE in the exp2 domain (lse2 = LSE *
+//   * fa_bwd_prep_kernel: -D_i and -LSE in the exp2 domain (lse2 = LSE *
 //     log2 e; +inf for rows with no visible key, so their P is 0), into
-//     row-padded workspace rows;
+//     row-padded workspace rows. They are stored negated because the
+//     rebuilds add them (one packed f32x2 add or FMA per two entries);
 //   * fa_bwd_dkdv_kernel: one CTA per 128-key tile of one (b, h). It keeps K
 //     and V in shared memory, streams (Q_i, dO_i, lse2_i, D_i) for every
 //     query tile that sees the key tile, forms S^T = K Q_i^T and
-//     dP^T = V dO_i^T with tcgen05 MMAs into tensor memory, lets one thread
-//     per key rebuild P^T and dS^T (bf16, written back over their own TMEM
-//     columns), and accumulates dV += P^T dO_i and dK += dS^T Q_i with the A
-//     operand read from TMEM;
+//     dP^T = V dO_i^T with 128-wide tcgen05 MMAs into tensor memory, lets
+//     the math warps rebuild P^T (once S^T lands) and dS^T (once dP^T lands)
+//     as bf16 written back over their own TMEM columns, and accumulates
+//     dV += P^T dO_i and dK += dS^T Q_i with the A operand read from TMEM.
+//     The MMAs are issued as dP(i) | dV(i) S(i+1) | dK(i) dP(i+1) | ..., so
+//     each rebuild runs while two other MMAs of the tile pipeline execute;
 //   * fa_bwd_dq_kernel: one CTA per 128-row query tile; for every key tile
 //     it sees: S = Q K_j^T, dP = dO V_j^T, then one thread per query rebuilds
-//     dS and dQ += dS K_j (A from TMEM).
-// Both gradient kernels split each 128-column score tile into two halves of
-// 64 columns with their own barriers: the MMA warp issues half 0's scores,
-// then half 1's; warps 0-3 rebuild half 0 while the tensor core computes
-// half 1, and half 0's gradient MMAs run while warps 4-7 rebuild half 1.
-// The two warps of a sub-partition share TMEM lanes (lane quarter = warp
-// mod 4) and split the columns. Each half packs its bf16 result into its own
-// first 32 columns (0-31 and 64-95), so neither half overwrites columns the
-// other has yet to read.
+//     dS and dQ += dS K_j (A from TMEM). Its score tile is split into two
+//     halves of 64 columns with their own barriers: the MMA warp issues half
+//     0's scores, then half 1's; warps 0-3 rebuild half 0 while the tensor
+//     core computes half 1.
+// An MMA of N = 64 columns takes about 0.84 of the time of one of N = 128
+// (measured: 54 against 64 cycles for M = 128, K = 16), so the 128-wide form
+// does the same work in 0.6 of the tensor time.
+// The math warps are 8: the two warps of a sub-partition share TMEM lanes
+// (lane quarter = warp mod 4) and split the columns; each packs its bf16
+// result into the first 32 of its 64 columns (0-31 and 64-95 of a region),
+// so neither overwrites columns the other has yet to read.
+// The dQ kernel is launched with programmatic stream serialization: its CTAs
+// start on the SMs the dK/dV kernel's last CTAs leave idle (it reads only
+// what the prep kernel wrote), and wait for the dK/dV grid before exiting, so
+// the launch as a whole still completes after both.
 // The warp roles, TMA ring, mbarrier waits (bounded) and descriptor
 // encodings are those of the forward kernel.
 #include <cmath>
@@ -53,8 +62,8 @@ struct Params {
     int Sq, Sk, Sq_pad, BH, n_qtiles, n_ktiles;
     int causal;
     float scale, scale_log2;
-    const float *lse2;  // [BH, Sq_pad], +inf padding
-    const float *Dvec;  // [BH, Sq_pad], 0 padding
+    const float *lse2;  // -lse2: [BH, Sq_pad], -inf padding
+    const float *Dvec;  // -D: [BH, Sq_pad], -0 padding
     unsigned int *status;
 };
 
@@ -103,14 +112,172 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int off = 16; off > 0; off /= 2)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        Dvec[row] = acc;
-        lse2[row] = l2;
+    if (lane == 0) {  // stored negated: the rebuilds add them
+        Dvec[row] = -acc;
+        lse2[row] = -l2;
     }
 }
 
 // Pack two fp32 values as a bf16 pair (element 2c in the low half).
 __device__ __forceinline__ uint32_t pk2(float a, float b) { return pack_bf16x2(a, b); }
+
+// 32 columns at `a` into r[0..31] and 32 columns at `b` into r[32..63], with
+// one wait (one asm statement, so no use of r can move above the wait).
+__device__ __forceinline__ void tmem_ld32x2_wait(uint32_t a, uint32_t b, uint32_t (&r)[64])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(a), "r"(b)
+        : "memory");
+}
+
+// The same two loads without the wait: r is valid only after ld_wait(r).
+__device__ __forceinline__ void tmem_ld32x2(uint32_t a, uint32_t b, uint32_t (&r)[64])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(a), "r"(b)
+        : "memory");
+}
+
+// Wait for this thread's TMEM loads. r is an operand (read and written), so
+// the compiler keeps every use of the loaded registers after the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[64])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]),
+                   "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]),
+                   "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]),
+                   "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]),
+                   "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]),
+                   "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b)
+{
+    return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+
+// 32 columns at `a` into r, without the wait: r is valid only after
+// tmem_ld_wait_regs32(r).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t a, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(a)
+        : "memory");
+}
+
+// Wait for this thread's TMEM loads; r is an operand (read and written), so
+// every use of the loaded registers stays after the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs32(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// P^T for one 32-column chunk of one key (this thread's TMEM lane):
+// P^T = 2^(S^T sl2 + nl), nl = -lse2 of the query (nl: the chunk's 32
+// queries, 16-byte aligned). The fp32 values go to pv, bf16 pairs to pp.
+// kMask zeroes the entries where `keep` is false.
+template <bool kMask, typename Keep>
+__device__ __forceinline__ void rebuild_p(const uint32_t (&st)[32], float2 sl2, const float *nl,
+                                          Keep keep, float *pv, uint32_t (&pp)[16])
+{
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4 *>(nl + c);
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            const float2 x = ffma2(f2(st[c + e], st[c + e + 1]), sl2,
+                                   e == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w));
+            float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            if (kMask) {
+                if (!keep(c + e))
+                    p0 = 0.0f;
+                if (!keep(c + e + 1))
+                    p1 = 0.0f;
+            }
+            pv[c + e] = p0;
+            pv[c + e + 1] = p1;
+            pp[(c + e) / 2] = pk2(p0, p1);
+        }
+    }
+}
+
+// dS^T = P^T (dP^T + nd), nd = -D of the query, for one 32-column chunk, as
+// bf16 pairs.
+__device__ __forceinline__ void rebuild_ds(const uint32_t (&dt)[32], const float *pv,
+                                           const float *nd, uint32_t (&pd)[16])
+{
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+        const float4 d4 = *reinterpret_cast<const float4 *>(nd + c);
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            const float2 ds = fmul2(
+                make_float2(pv[c + e], pv[c + e + 1]),
+                fadd2(f2(dt[c + e], dt[c + e + 1]),
+                      e == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w)));
+            pd[(c + e) / 2] = pk2(ds.x, ds.y);
+        }
+    }
+}
 
 // The epilogue of both gradient kernels: a 128 x D fp32 tile in TMEM (this
 // thread's lane = row r; `taddr` addresses column 0 of that lane) times
@@ -172,8 +339,8 @@ struct KvCfg {
 struct KvBars {
     uint64_t kv_full;
     uint64_t full[4], empty[4];
-    uint64_t st_full[2];  // half h of S^T and dP^T of the current query tile in TMEM
-    uint64_t p_full[2];   // half h of P^T and dS^T written back (4 warp arrivals)
+    uint64_t s_full, dp_full;  // S^T / dP^T of the current query tile in TMEM
+    uint64_t p_full, ds_full;  // P^T / dS^T written back (8 warp arrivals each)
     uint64_t o_done;   // last dV / dK MMAs completed
     uint64_t drain;
     uint32_t tmem_base;
@@ -194,9 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     KvBars *bars = reinterpret_cast<KvBars *>(smem + C::kOffBar);
+    // The dQ grid may start on SMs this grid no longer needs.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x / p.n_ktiles;
-    const int kt = p.n_ktiles - 1 - static_cast<int>(blockIdx.x % p.n_ktiles);  // long first
+    const int kt = static_cast<int>(blockIdx.x % p.n_ktiles);  // long first
     const int kv0 = kt * kBlock;
     const int off = p.Sk - p.Sq;
     // Query tiles whose last row sees key kv0: [qt0, n_qtiles).
@@ -213,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        for (int h = 0; h < 2; ++h) {
-            mbar_init(&bars->st_full[h], 1);
-            mbar_init(&bars->p_full[h], 4);
-        }
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->dp_full, 1);
+        mbar_init(&bars->p_full, kMathThreads / 32);
+        mbar_init(&bars->ds_full, kMathThreads / 32);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
@@ -262,70 +431,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0 && n_q > 0) {
-            constexpr uint32_t idesc_h = idesc_bf16_f32(kBlock, kHalf, false, false);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlock, kBlock, false, false);
             constexpr uint32_t idesc_g = idesc_bf16_f32(kBlock, D, false, true);
             const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
             const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
             const uint32_t ring = smem_u32(smem + C::kOffRing);
-            // Half h of S^T = K Q^T and dP^T = V dO^T: the query rows
-            // [64h, 64h + 64) of the tile (both operands K-major).
-            auto issue_scores = [&](int n, int h) {
-                const uint32_t sq = ring + (n % C::kStages) * C::kStageBytes + h * kHalf * 128;
-                const uint64_t dq0 = smem_desc_sw128(sq, 16, 1024);
-                const uint64_t ddo0 = smem_desc_sw128(sq + C::kTile, 16, 1024);
+            // S^T = K Q^T (A = K, B = Q, both K-major), or dP^T = V dO^T,
+            // over the tile's 128 queries.
+            auto issue_scores = [&](int n, bool dp) {
+                const uint32_t sq = ring + (n % C::kStages) * C::kStageBytes + (dp ? C::kTile : 0);
+                const uint64_t b0 = smem_desc_sw128(sq, 16, 1024);
+                const uint64_t a0 = dp ? dv0 : dk0;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColS + h * kHalf, dk0 + koff, dq0 + koff, idesc_h,
-                                 kk > 0);
+                    umma_bf16_ss(tmem + (dp ? C::kColDP : C::kColS), a0 + koff, b0 + koff,
+                                 idesc_s, kk > 0);
                 }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColDP + h * kHalf, dv0 + koff, ddo0 + koff, idesc_h,
-                                 kk > 0);
-                }
-                umma_commit(&bars->st_full[h]);
+                umma_commit(dp ? &bars->dp_full : &bars->s_full);
             };
-            // dV += P^T dO and dK += dS^T Q over the query rows of half h:
-            // A (bf16 pairs) from the half's first 32 TMEM columns, B (dO, Q)
-            // MN-major from shared memory.
-            auto issue_grads = [&](int n, int h) {
-                const uint32_t sq = ring + (n % C::kStages) * C::kStageBytes;
-                const uint64_t bq = smem_desc_sw128(sq, kBoxBytes, 1024);
-                const uint64_t bdo = smem_desc_sw128(sq + C::kTile, kBoxBytes, 1024);
+            // dV += P^T dO (A = P^T from the S columns) or dK += dS^T Q (A =
+            // dS^T from the dP columns). A is bf16 pairs: queries 0-63 in the
+            // region's columns 0-31, queries 64-127 in columns 64-95. B (dO,
+            // Q) MN-major from shared memory.
+            auto issue_grad = [&](int n, bool dk) {
+                const uint32_t sq = ring + (n % C::kStages) * C::kStageBytes + (dk ? 0 : C::kTile);
+                const uint64_t b0 = smem_desc_sw128(sq, kBoxBytes, 1024);
+                const uint32_t a0 = tmem + (dk ? C::kColDP : C::kColS);
 #pragma unroll
-                for (int k4 = 0; k4 < kHalf / 16; ++k4) {
-                    const int kk = h * (kHalf / 16) + k4;
-                    umma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + h * kHalf + k4 * 8,
-                                 bdo + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
+                for (int kk = 0; kk < kBlock / 16; ++kk)
+                    umma_bf16_ts(tmem + (dk ? C::kColDK : C::kColDV),
+                                 a0 + (kk / 4) * kHalf + (kk % 4) * 8,
+                                 b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (n > 0 || kk > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int k4 = 0; k4 < kHalf / 16; ++k4) {
-                    const int kk = h * (kHalf / 16) + k4;
-                    umma_bf16_ts(tmem + C::kColDK, tmem + C::kColDP + h * kHalf + k4 * 8,
-                                 bq + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
-                                 (n > 0 || kk > 0) ? 1u : 0u);
-                }
             };
             bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.status) &&
                       mbar_wait(&bars->full[0], 0, abort_flag, p.status);
             if (ok) {
                 tc_fence_after_sync();
-                issue_scores(0, 0);
-                issue_scores(0, 1);
+                issue_scores(0, false);
+                issue_scores(0, true);
             }
-            // Tile n+1's half-0 scores are issued between tile n's two
-            // gradient halves, so the tensor core has work while either
-            // group of math warps is busy. MMAs from one thread run in
-            // issue order, which orders each TMEM reuse after its reader.
+            // Issue order: ... dP(n) | dV(n) S(n+1) | dK(n) dP(n+1) | dV(n+1) ...
+            // Each rebuild (P^T after S^T lands, dS^T after dP^T lands) has
+            // two 128-wide MMAs ahead of the one that consumes it. MMAs from
+            // one thread run in issue order, which orders each TMEM reuse
+            // after its reader; the math warps read S^T (dP^T) before they
+            // signal P^T (dS^T).
             for (int n = 0; n < n_q && ok; ++n) {
-                ok = mbar_wait(&bars->p_full[0], n & 1, abort_flag, p.status);
+                ok = mbar_wait(&bars->p_full, n & 1, abort_flag, p.status);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
-                issue_grads(n, 0);
+                issue_grad(n, false);
                 const bool next = n + 1 < n_q;
                 if (next) {
                     ok = mbar_wait(&bars->full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1,
@@ -333,16 +491,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok)
                         break;
                     tc_fence_after_sync();
-                    issue_scores(n + 1, 0);
+                    issue_scores(n + 1, false);
                 }
-                ok = mbar_wait(&bars->p_full[1], n & 1, abort_flag, p.status);
+                ok = mbar_wait(&bars->ds_full, n & 1, abort_flag, p.status);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
-                issue_grads(n, 1);
+                issue_grad(n, true);
                 umma_commit(&bars->empty[n % C::kStages]);
                 if (next)
-                    issue_scores(n + 1, 1);
+                    issue_scores(n + 1, true);
             }
             umma_commit(&bars->o_done);
             umma_commit(&bars->drain);
@@ -356,11 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_base + C::kColS + half * kHalf;
         const uint32_t tDP = tmem + lane_base + C::kColDP + half * kHalf;
-        const float sl2 = p.scale_log2;
+        const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int n = 0; n < n_q && ok; ++n) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->st_full[half], n & 1, abort_flag, p.status));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, n & 1, abort_flag, p.status));
             if (!ok)
                 break;
             tc_fence_after_sync();
@@ -370,37 +527,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                                half * kHalf;
             // mask: key beyond Sk, or (causal) key after the query's last visible key
             const bool tile_masked = key >= p.Sk || (p.causal && kv0 + kBlock - 1 > q0 + off);
+            // P^T = 2^(S^T sl2 - lse2) for this thread's 64 queries, kept in
+            // fp32 for dS^T. Chunk 1's loads are in flight while chunk 0 is
+            // rebuilt.
+            float pv[kHalf];
+            {
+                uint32_t sd[2][kChunk];
+                tmem_ld32_wait(tS, sd[0]);
+                tmem_ld32_nowait(tS + kChunk, sd[1]);
 #pragma unroll
-            for (int c0 = 0; c0 < kHalf; c0 += kChunk) {
-                uint32_t sr[kChunk], dr[kChunk];
-                tmem_ld32_wait(tS + c0, sr);
-                tmem_ld32_wait(tDP + c0, dr);
-                uint32_t pp[kChunk / 2], pd[kChunk / 2];
-#pragma unroll
-                for (int c = 0; c < kChunk; c += 2) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int qc = c0 + c + e;
-                        float pr = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -vec[qc]));
-                        if (tile_masked &&
-                            (key >= p.Sk || (p.causal && key > q0 + qc + off)))
-                            pr = 0.0f;
-                        pv[e] = pr;
-                        dv[e] = pr * (__uint_as_float(dr[c + e]) - vec[128 + qc]);
+                for (int ch = 0; ch < kHalf / kChunk; ++ch) {
+                    const int c0 = ch * kChunk;
+                    if (ch > 0)
+                        tmem_ld_wait_regs32(sd[ch]);
+                    uint32_t pp[kChunk / 2];
+                    if (!tile_masked) {
+                        rebuild_p<false>(sd[ch], sl2x2, vec + c0, [](int) { return true; },
+                                         pv + c0, pp);
+                    } else {
+                        const int lim = q0 + c0 + off;  // query of column c sees key <= lim + c
+                        const bool in_k = key < p.Sk;
+                        rebuild_p<true>(sd[ch], sl2x2, vec + c0,
+                                        [&](int c) { return in_k && (!p.causal || key <= lim + c); },
+                                        pv + c0, pp);
                     }
-                    pp[c / 2] = pk2(pv[0], pv[1]);
-                    pd[c / 2] = pk2(dv[0], dv[1]);
+                    tmem_st16(tS + c0 / 2, pp);  // over this half's own, already read columns
                 }
-                // P^T and dS^T (bf16 pairs) over this half's own, already read columns
-                tmem_st16(tS + c0 / 2, pp);
-                tmem_st16(tDP + c0 / 2, pd);
             }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bars->p_full[half]);
+                mbar_arrive(&bars->p_full);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full, n & 1, abort_flag, p.status));
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            // dS^T = P^T (dP^T - D)
+            {
+                uint32_t sd[2][kChunk];
+                tmem_ld32_wait(tDP, sd[0]);
+                tmem_ld32_nowait(tDP + kChunk, sd[1]);
+#pragma unroll
+                for (int ch = 0; ch < kHalf / kChunk; ++ch) {
+                    const int c0 = ch * kChunk;
+                    if (ch > 0)
+                        tmem_ld_wait_regs32(sd[ch]);
+                    uint32_t pd[kChunk / 2];
+                    rebuild_ds(sd[ch], pv + c0, vec + 128 + c0, pd);
+                    tmem_st16(tDP + c0 / 2, pd);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->ds_full);
         }
         // ------------------------------------------------------------ epilogue
         if (ok && n_q > 0) {
@@ -430,6 +612,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
+// One 32-column chunk of the dQ kernel's rebuild for one query (this
+// thread's TMEM lane): P = 2^(S sl2 + nl) (nl = -lse2 of the query),
+// dS = P (dP + nd) (nd = -D), as bf16 pairs. sd holds S in 0-31 and dP in
+// 32-63. kMask zeroes the columns c >= n_vis.
+template <bool kMask>
+__device__ __forceinline__ void rebuild_dq_chunk(const uint32_t (&sd)[64], float2 sl2, float2 nl,
+                                                 float2 nd, int n_vis, uint32_t (&pd)[16])
+{
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+        const float2 x = ffma2(f2(sd[c], sd[c + 1]), sl2, nl);
+        float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (kMask) {
+            if (c >= n_vis)
+                pv.x = 0.0f;
+            if (c + 1 >= n_vis)
+                pv.y = 0.0f;
+        }
+        const float2 ds = fmul2(pv, fadd2(f2(sd[32 + c], sd[32 + c + 1]), nd));
+        pd[c / 2] = pk2(ds.x, ds.y);
+    }
+}
+
 template <int D>
 struct QCfg {
     static constexpr int kTile = kBlock * D * 2;
@@ -607,9 +812,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_base + C::kColS + half * kHalf;
         const uint32_t tDP = tmem + lane_base + C::kColDP + half * kHalf;
-        const float sl2 = p.scale_log2;
+        const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
         const size_t vrow = static_cast<size_t>(bh) * p.Sq_pad + i;
-        const float l2 = p.lse2[vrow], Di = p.Dvec[vrow];  // padded rows: +inf, 0
+        // -lse2 and -D of this query (padded rows: -inf, -0)
+        const float2 nl2 = make_float2(p.lse2[vrow], p.lse2[vrow]);
+        const float2 nD = make_float2(p.Dvec[vrow], p.Dvec[vrow]);
         const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
         bool ok = true;
         for (int j = 0; j < n_kv && ok; ++j) {
@@ -620,24 +827,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const bool tile_masked = j >= mask_from;
             const int key0 = j * kBlock + half * kHalf;  // first key of this half
+            uint32_t sd[2][2 * kChunk];
+            tmem_ld32x2_wait(tS, tDP, sd[0]);
+            tmem_ld32x2(tS + kChunk, tDP + kChunk, sd[1]);
 #pragma unroll
-            for (int c0 = 0; c0 < kHalf; c0 += kChunk) {
-                uint32_t sr[kChunk], dr[kChunk];
-                tmem_ld32_wait(tS + c0, sr);
-                tmem_ld32_wait(tDP + c0, dr);
+            for (int ch = 0; ch < kHalf / kChunk; ++ch) {
+                const int c0 = ch * kChunk;
+                if (ch > 0)
+                    tmem_ld_wait_regs(sd[ch]);
                 uint32_t pd[kChunk / 2];
-#pragma unroll
-                for (int c = 0; c < kChunk; c += 2) {
-                    float ds[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float pr = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -l2));
-                        if (tile_masked && key0 + c0 + c + e >= lim)
-                            pr = 0.0f;
-                        ds[e] = pr * (__uint_as_float(dr[c + e]) - Di);
-                    }
-                    pd[c / 2] = pk2(ds[0], ds[1]);
-                }
+                if (!tile_masked)
+                    rebuild_dq_chunk<false>(sd[ch], sl2x2, nl2, nD, 0, pd);
+                else
+                    rebuild_dq_chunk<true>(sd[ch], sl2x2, nl2, nD, lim - (key0 + c0), pd);
                 tmem_st16(tS + c0 / 2, pd);  // dS (bf16 pairs) over this half's read columns
             }
             tmem_st_wait();
@@ -665,6 +867,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     if (warp == kMmaWarp)
         tmem_dealloc(tmem, kTmemCols);
+    // Complete only after the dK/dV grid (this grid's programmatic
+    // predecessor), so work queued after the backward sees dK and dV.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D>
@@ -726,9 +931,17 @@ fa_status_t launch(const BackwardProblem &bp)
         const uint64_t grid = static_cast<uint64_t>(p.n_qtiles) * BH;
         if (grid > 0x7FFFFFFFull)
             return FA_ERR_UNSUPPORTED;
-        kern<<<static_cast<unsigned>(grid), kThreads, QCfg<D>::kSmem, pr.stream>>>(tq, tk, tv, tdo,
-                                                                                 tdq, p);
-        if (cudaGetLastError() != cudaSuccess)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = QCfg<D>::kSmem;
+        cfg.stream = pr.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tdq, p) != cudaSuccess)
             return FA_ERR_CUDA;
     }
     return FA_OK;
