@@ -22,14 +22,14 @@
 //     The MMAs are issued as dP(i) | dV(i) S(i+1) | dK(i) dP(i+1) | ..., so
 //     each rebuild runs while two other MMAs of the tile pipeline execute;
 //   * fa_bwd_dq_kernel: one CTA per 128-row query tile; for every key tile
-//     it sees: S = Q K_j^T, dP = dO V_j^T, then one thread per query rebuilds
-//     dS and dQ += dS K_j (A from TMEM). Its score tile is split into two
-//     halves of 64 columns with their own barriers: the MMA warp issues half
-//     0's scores, then half 1's; warps 0-3 rebuild half 0 while the tensor
-//     core computes half 1.
-// An MMA of N = 64 columns takes about 0.84 of the time of one of N = 128
-// (measured: 54 against 64 cycles for M = 128, K = 16), so the 128-wide form
-// does the same work in 0.6 of the tensor time.
+//     it sees: S = Q K_j^T (two TMEM buffers), dP = dO V_j^T, then the math
+//     warps rebuild P (fp32, in registers) once S lands and dS once dP
+//     lands, written back as bf16 over dP's columns, and dQ += dS K_j (A
+//     from TMEM). Issue order S(j+1) | dQ(j) dP(j+1) S(j+2) | ..., with K
+//     in a 3-deep ring of its own (K_j is read by S(j) and again by dQ(j)).
+// All score MMAs are 128 wide: an M = 128 MMA of N = 64 columns takes 54
+// cycles against 64 for N = 128 (K = 16, measured), so two 64-wide halves
+// take 1.7x the tensor time of one 128-wide MMA.
 // The math warps are 8: the two warps of a sub-partition share TMEM lanes
 // (lane quarter = warp mod 4) and split the columns; each packs its bf16
 // result into the first 32 of its 64 columns (0-31 and 64-95 of a region),
@@ -120,78 +120,6 @@ __global__ void __launch_bounds__(256)
 
 // Pack two fp32 values as a bf16 pair (element 2c in the low half).
 __device__ __forceinline__ uint32_t pk2(float a, float b) { return pack_bf16x2(a, b); }
-
-// 32 columns at `a` into r[0..31] and 32 columns at `b` into r[32..63], with
-// one wait (one asm statement, so no use of r can move above the wait).
-__device__ __forceinline__ void tmem_ld32x2_wait(uint32_t a, uint32_t b, uint32_t (&r)[64])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
-          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
-          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
-          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
-          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
-          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(a), "r"(b)
-        : "memory");
-}
-
-// The same two loads without the wait: r is valid only after ld_wait(r).
-__device__ __forceinline__ void tmem_ld32x2(uint32_t a, uint32_t b, uint32_t (&r)[64])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
-          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
-          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
-          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
-          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
-          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(a), "r"(b)
-        : "memory");
-}
-
-// Wait for this thread's TMEM loads. r is an operand (read and written), so
-// the compiler keeps every use of the loaded registers after the wait.
-__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[64])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                   "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]),
-                   "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]),
-                   "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]),
-                   "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]),
-                   "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]),
-                   "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
-                 :
-                 : "memory");
-}
 
 __device__ __forceinline__ float2 f2(uint32_t a, uint32_t b)
 {
@@ -612,44 +540,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
-// One 32-column chunk of the dQ kernel's rebuild for one query (this
-// thread's TMEM lane): P = 2^(S sl2 + nl) (nl = -lse2 of the query),
-// dS = P (dP + nd) (nd = -D), as bf16 pairs. sd holds S in 0-31 and dP in
-// 32-63. kMask zeroes the columns c >= n_vis.
+// P = 2^(S sl2 + nl) (nl = -lse2 of this thread's query) for one 32-column
+// chunk, into pv. kMask zeroes the columns c >= n_vis.
 template <bool kMask>
-__device__ __forceinline__ void rebuild_dq_chunk(const uint32_t (&sd)[64], float2 sl2, float2 nl,
-                                                 float2 nd, int n_vis, uint32_t (&pd)[16])
+__device__ __forceinline__ void rebuild_q_p(const uint32_t (&st)[32], float2 sl2, float2 nl,
+                                            int n_vis, float *pv)
 {
 #pragma unroll
     for (int c = 0; c < 32; c += 2) {
-        const float2 x = ffma2(f2(sd[c], sd[c + 1]), sl2, nl);
-        float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        const float2 x = ffma2(f2(st[c], st[c + 1]), sl2, nl);
+        float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
         if (kMask) {
             if (c >= n_vis)
-                pv.x = 0.0f;
+                p0 = 0.0f;
             if (c + 1 >= n_vis)
-                pv.y = 0.0f;
+                p1 = 0.0f;
         }
-        const float2 ds = fmul2(pv, fadd2(f2(sd[32 + c], sd[32 + c + 1]), nd));
+        pv[c] = p0;
+        pv[c + 1] = p1;
+    }
+}
+
+// dS = P (dP + nd) (nd = -D of this thread's query) for one 32-column chunk,
+// as bf16 pairs.
+__device__ __forceinline__ void rebuild_q_ds(const uint32_t (&dt)[32], const float *pv, float2 nd,
+                                             uint32_t (&pd)[16])
+{
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+        const float2 ds = fmul2(make_float2(pv[c], pv[c + 1]), fadd2(f2(dt[c], dt[c + 1]), nd));
         pd[c / 2] = pk2(ds.x, ds.y);
     }
 }
 
+// K and V tiles sit in rings of their own: K_j is read by S(j) and, later,
+// by dQ(j); V_j only by dP(j), so K needs the deeper ring.
 template <int D>
 struct QCfg {
     static constexpr int kTile = kBlock * D * 2;
-    static constexpr int kStages = (D == 128) ? 2 : 4;  // (K_j, V_j) pairs
-    static constexpr int kOffQ = 0, kOffDO = kTile, kOffRing = 2 * kTile;
-    static constexpr int kStageBytes = 2 * kTile;
-    static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+    static constexpr int kKStages = (D == 128) ? 3 : 4;
+    static constexpr int kVStages = (D == 128) ? 2 : 4;
+    static constexpr int kOffQ = 0, kOffDO = kTile, kOffK = 2 * kTile;
+    static constexpr int kOffV = kOffK + kKStages * kTile;
+    static constexpr int kOffBar = kOffV + kVStages * kTile;
     static constexpr int kSmem = kOffBar + 512 + 1024;
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+    // Two S buffers (S(j) in buffer j % 2), dP, dQ.
+    static constexpr uint32_t kColS0 = 0, kColDP = 128, kColDQ = 256, kColS1 = 384;
+    static_assert(kColDQ + D <= kColS1, "TMEM budget");
 };
 
 struct QBars {
     uint64_t q_full;
-    uint64_t full[4], empty[4];
-    uint64_t st_full[2], p_full[2];  // per column half, as in KvBars
+    uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+    uint64_t s_full[2];  // S(j) in buffer j % 2
+    uint64_t dp_full;    // dP(j) in TMEM
+    uint64_t ds_full;    // dS(j) written back (8 warp arrivals)
     uint64_t o_done, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -678,14 +623,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
         }
-        for (int h = 0; h < 2; ++h) {
-            mbar_init(&bars->st_full[h], 1);
-            mbar_init(&bars->p_full[h], 4);
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
         }
+        mbar_init(&bars->s_full[0], 1);
+        mbar_init(&bars->s_full[1], 1);
+        mbar_init(&bars->dp_full, 1);
+        mbar_init(&bars->ds_full, kMathThreads / 32);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
@@ -711,95 +660,128 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(smem + C::kOffQ + b * kBoxBytes, &tm_q, &bars->q_full, b * 64, q0, bh);
                 tma_load_3d(smem + C::kOffDO + b * kBoxBytes, &tm_do, &bars->q_full, b * 64, q0, bh);
             }
+            // K_j then V_j: V_j's slot frees (dP(j - kVStages) done) before
+            // K_{j+1}'s (dQ(j + 1 - kKStages) done), so neither wait holds
+            // up a copy that could already start.
             int j = 0;
-            for (; j < n_kv; ++j) {
-                const int s = j % C::kStages;
-                const uint32_t use = j / C::kStages;
-                if (use > 0 && !mbar_wait(&bars->empty[s], (use - 1) & 1, abort_flag, p.status))
+            bool ok = true;
+            for (; j < n_kv && ok; ++j) {
+                const int sk = j % C::kKStages, sv = j % C::kVStages;
+                const uint32_t uk = j / C::kKStages, uv = j / C::kVStages;
+                if (uk > 0 && !mbar_wait(&bars->k_empty[sk], (uk - 1) & 1, abort_flag, p.status))
                     break;
-                uint8_t *st = smem + C::kOffRing + s * C::kStageBytes;
-                mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
-                for (int b = 0; b < D / 64; ++b) {
-                    tma_load_3d(st + b * kBoxBytes, &tm_k, &bars->full[s], b * 64, j * kBlock, bh);
-                    tma_load_3d(st + C::kTile + b * kBoxBytes, &tm_v, &bars->full[s], b * 64,
-                                j * kBlock, bh);
+                mbar_arrive_expect_tx(&bars->k_full[sk], C::kTile);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(smem + C::kOffK + sk * C::kTile + b * kBoxBytes, &tm_k,
+                                &bars->k_full[sk], b * 64, j * kBlock, bh);
+                if (uv > 0 && !mbar_wait(&bars->v_empty[sv], (uv - 1) & 1, abort_flag, p.status)) {
+                    ok = false;  // K_j is in flight: drain it below
+                    ++j;
+                    break;
                 }
+                mbar_arrive_expect_tx(&bars->v_full[sv], C::kTile);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(smem + C::kOffV + sv * C::kTile + b * kBoxBytes, &tm_v,
+                                &bars->v_full[sv], b * 64, j * kBlock, bh);
             }
+            // Drain the copies in flight (at most the last ring's worth of each).
             mbar_wait_drain(&bars->q_full, 0, p.status);
-            for (int k = max(0, j - C::kStages); k < j; ++k)
-                mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status);
+            const int nk = j, nv = ok ? j : j - 1;
+            for (int k = max(0, nk - C::kKStages); k < nk; ++k)
+                mbar_wait_drain(&bars->k_full[k % C::kKStages], (k / C::kKStages) & 1, p.status);
+            for (int k = max(0, nv - C::kVStages); k < nv; ++k)
+                mbar_wait_drain(&bars->v_full[k % C::kVStages], (k / C::kVStages) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0 && n_kv > 0) {
-            constexpr uint32_t idesc_h = idesc_bf16_f32(kBlock, kHalf, false, false);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlock, kBlock, false, false);
             constexpr uint32_t idesc_g = idesc_bf16_f32(kBlock, D, false, true);
             const uint64_t aq0 = smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
             const uint64_t ado0 = smem_desc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
-            const uint32_t ring = smem_u32(smem + C::kOffRing);
-            // Half h of S = Q K^T and dP = dO V^T: the keys [64h, 64h + 64)
-            // of the tile (both operands K-major).
-            auto issue_scores = [&](int j, int h) {
-                const uint32_t sk = ring + (j % C::kStages) * C::kStageBytes + h * kHalf * 128;
-                const uint64_t bk0 = smem_desc_sw128(sk, 16, 1024);
-                const uint64_t bv0 = smem_desc_sw128(sk + C::kTile, 16, 1024);
+            const uint32_t kring = smem_u32(smem + C::kOffK), vring = smem_u32(smem + C::kOffV);
+            // S(j) = Q K_j^T into buffer j % 2, or dP(j) = dO V_j^T: 128 keys,
+            // both operands K-major.
+            auto issue_scores = [&](int j, bool dp) {
+                const uint32_t sb = dp ? vring + (j % C::kVStages) * C::kTile
+                                       : kring + (j % C::kKStages) * C::kTile;
+                const uint64_t b0 = smem_desc_sw128(sb, 16, 1024);
+                const uint64_t a0 = dp ? ado0 : aq0;
+                const uint32_t col = dp ? C::kColDP : ((j & 1) ? C::kColS1 : C::kColS0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColS + h * kHalf, aq0 + koff, bk0 + koff, idesc_h,
-                                 kk > 0);
+                    umma_bf16_ss(tmem + col, a0 + koff, b0 + koff, idesc_s, kk > 0);
                 }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + C::kColDP + h * kHalf, ado0 + koff, bv0 + koff, idesc_h,
-                                 kk > 0);
+                if (dp) {
+                    umma_commit(&bars->dp_full);
+                    umma_commit(&bars->v_empty[j % C::kVStages]);
+                } else {
+                    umma_commit(&bars->s_full[j & 1]);
                 }
-                umma_commit(&bars->st_full[h]);
             };
-            // dQ += dS K over the keys of half h: A = dS (bf16 pairs) from
-            // the half's first 32 TMEM columns, B = K MN-major.
-            auto issue_grad = [&](int j, int h) {
-                const uint32_t sk = ring + (j % C::kStages) * C::kStageBytes;
+            // dQ += dS K_j: A = dS (bf16 pairs: keys 0-63 in the dP region's
+            // columns 0-31, keys 64-127 in 64-95), B = K_j MN-major.
+            auto issue_grad = [&](int j) {
+                const uint32_t sk = kring + (j % C::kKStages) * C::kTile;
                 const uint64_t bkm = smem_desc_sw128(sk, kBoxBytes, 1024);
 #pragma unroll
-                for (int k4 = 0; k4 < kHalf / 16; ++k4) {
-                    const int kk = h * (kHalf / 16) + k4;
-                    umma_bf16_ts(tmem + C::kColDQ, tmem + C::kColS + h * kHalf + k4 * 8,
+                for (int kk = 0; kk < kBlock / 16; ++kk)
+                    umma_bf16_ts(tmem + C::kColDQ, tmem + C::kColDP + (kk / 4) * kHalf + (kk % 4) * 8,
                                  bkm + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                umma_commit(&bars->k_empty[j % C::kKStages]);
             };
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status) &&
-                      mbar_wait(&bars->full[0], 0, abort_flag, p.status);
+            auto wait_k = [&](int j) {
+                return mbar_wait(&bars->k_full[j % C::kKStages], (j / C::kKStages) & 1, abort_flag,
+                                 p.status);
+            };
+            auto wait_v = [&](int j) {
+                return mbar_wait(&bars->v_full[j % C::kVStages], (j / C::kVStages) & 1, abort_flag,
+                                 p.status);
+            };
+            // Issue order: S(0) dP(0) S(1) | dQ(0) dP(1) S(2) | dQ(1) dP(2) S(3) | ...
+            // dS(j) is rebuilt while dP(j)'s successors S(j+1) (and the
+            // previous dQ) execute. dP(j+1) reuses dP's columns after dQ(j)
+            // read dS(j) from them, and S(j+2) reuses S(j)'s buffer; MMAs
+            // from one thread run in issue order, and the math warps read
+            // S(j) and dP(j) before they signal dS(j).
+            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status) && wait_k(0);
             if (ok) {
                 tc_fence_after_sync();
-                issue_scores(0, 0);
-                issue_scores(0, 1);
+                issue_scores(0, false);
+                ok = wait_v(0);
             }
-            // The same interleaving as the dK/dV kernel.
+            if (ok) {
+                tc_fence_after_sync();
+                issue_scores(0, true);
+                if (n_kv > 1) {
+                    ok = wait_k(1);
+                    if (ok) {
+                        tc_fence_after_sync();
+                        issue_scores(1, false);
+                    }
+                }
+            }
             for (int j = 0; j < n_kv && ok; ++j) {
-                ok = mbar_wait(&bars->p_full[0], j & 1, abort_flag, p.status);
+                ok = mbar_wait(&bars->ds_full, j & 1, abort_flag, p.status);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
-                issue_grad(j, 0);
-                const bool next = j + 1 < n_kv;
-                if (next) {
-                    ok = mbar_wait(&bars->full[(j + 1) % C::kStages], ((j + 1) / C::kStages) & 1,
-                                   abort_flag, p.status);
+                issue_grad(j);
+                if (j + 1 < n_kv) {
+                    ok = wait_v(j + 1);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
-                    issue_scores(j + 1, 0);
+                    issue_scores(j + 1, true);
                 }
-                ok = mbar_wait(&bars->p_full[1], j & 1, abort_flag, p.status);
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-                issue_grad(j, 1);
-                umma_commit(&bars->empty[j % C::kStages]);
-                if (next)
-                    issue_scores(j + 1, 1);
+                if (j + 2 < n_kv) {
+                    ok = wait_k(j + 2);
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    issue_scores(j + 2, false);
+                }
             }
             umma_commit(&bars->o_done);
             umma_commit(&bars->drain);
@@ -810,7 +792,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
         const int i = q0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS + half * kHalf;
         const uint32_t tDP = tmem + lane_base + C::kColDP + half * kHalf;
         const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
         const size_t vrow = static_cast<size_t>(bh) * p.Sq_pad + i;
@@ -821,32 +802,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < n_kv && ok; ++j) {
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->st_full[half], j & 1, abort_flag, p.status));
+                            mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag, p.status));
             if (!ok)
                 break;
             tc_fence_after_sync();
             const bool tile_masked = j >= mask_from;
             const int key0 = j * kBlock + half * kHalf;  // first key of this half
-            uint32_t sd[2][2 * kChunk];
-            tmem_ld32x2_wait(tS, tDP, sd[0]);
-            tmem_ld32x2(tS + kChunk, tDP + kChunk, sd[1]);
+            const uint32_t tS = tmem + lane_base + ((j & 1) ? C::kColS1 : C::kColS0) + half * kHalf;
+            // P for this thread's 64 keys, in fp32 (loads of the second
+            // chunk in flight while the first is rebuilt)
+            float pv[kHalf];
+            {
+                uint32_t sd[2][kChunk];
+                tmem_ld32_wait(tS, sd[0]);
+                tmem_ld32_nowait(tS + kChunk, sd[1]);
 #pragma unroll
-            for (int ch = 0; ch < kHalf / kChunk; ++ch) {
-                const int c0 = ch * kChunk;
-                if (ch > 0)
-                    tmem_ld_wait_regs(sd[ch]);
-                uint32_t pd[kChunk / 2];
-                if (!tile_masked)
-                    rebuild_dq_chunk<false>(sd[ch], sl2x2, nl2, nD, 0, pd);
-                else
-                    rebuild_dq_chunk<true>(sd[ch], sl2x2, nl2, nD, lim - (key0 + c0), pd);
-                tmem_st16(tS + c0 / 2, pd);  // dS (bf16 pairs) over this half's read columns
+                for (int ch = 0; ch < kHalf / kChunk; ++ch) {
+                    const int c0 = ch * kChunk;
+                    if (ch > 0)
+                        tmem_ld_wait_regs32(sd[ch]);
+                    if (!tile_masked)
+                        rebuild_q_p<false>(sd[ch], sl2x2, nl2, 0, pv + c0);
+                    else
+                        rebuild_q_p<true>(sd[ch], sl2x2, nl2, lim - (key0 + c0), pv + c0);
+                }
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full, j & 1, abort_flag, p.status));
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            // dS = P (dP - D), as bf16 pairs over this half's first 32 dP columns
+            {
+                uint32_t sd[2][kChunk];
+                tmem_ld32_wait(tDP, sd[0]);
+                tmem_ld32_nowait(tDP + kChunk, sd[1]);
+#pragma unroll
+                for (int ch = 0; ch < kHalf / kChunk; ++ch) {
+                    const int c0 = ch * kChunk;
+                    if (ch > 0)
+                        tmem_ld_wait_regs32(sd[ch]);
+                    uint32_t pd[kChunk / 2];
+                    rebuild_q_ds(sd[ch], pv + c0, nD, pd);
+                    tmem_st16(tDP + c0 / 2, pd);
+                }
             }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bars->p_full[half]);
+                mbar_arrive(&bars->ds_full);
         }
         if (ok && n_kv > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abort_flag, p.status));
