@@ -258,6 +258,26 @@ def measure_exp_pipe(w, device, sptr):
             "tensor_ms_lower_bound": w.exact_flops() / 1917.5e12 * 1e3}
 
 
+MMA_FORMS = {0: "ss_n128", 1: "ss_2x_n64", 2: "ts_n128", 3: "ts_2x_n64", 4: "ss_n256"}
+
+
+def measure_mma_rate(device, sptr):
+    """SM cycles per 128 x 128 x 128 bf16 tcgen05 product in each operand form
+    (one CTA per SM, median over CTAs). 512 is the nominal dense rate."""
+    from exact_tiled_attention_03_gb300 import _capi
+
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    cyc = torch.empty(sms, dtype=torch.int64, device=device)
+    iters, out = 1000, {}
+    for mode, name in MMA_FORMS.items():
+        for _ in range(2):
+            _capi.check(_capi.fa_selftest_mma_rate(cyc, mode, sms, iters, sptr), "mma_rate")
+        torch.cuda.synchronize(device)
+        per = cyc.double().median().item() / (iters * (2 if mode == 4 else 1))
+        out[name] = round(per, 1)
+    return {"clk_per_128x128x128": out, "nominal": 512}
+
+
 def run_reference(args, world, rank):
     """--impl reference: the fp64 CPU oracle on the same workload, rank 0 only."""
     if rank != 0:
@@ -545,6 +565,7 @@ def run_ours(args, world, rank, local):
 
     # the exp-pipe bound of the prefill step (MUFU microbenchmark)
     exp_pipe = measure_exp_pipe(w, device, sptr)
+    mma_rate = measure_mma_rate(device, sptr)
 
     # the verify step's tree-mask and paged-cache forms, same bytes and roofline
     verify_ext = None
@@ -586,7 +607,7 @@ def run_ours(args, world, rank, local):
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
             "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "backward": backward,
-            "fp8": fp8, "exp_pipe": exp_pipe, "cpu_baseline": cpu,
+            "fp8": fp8, "exp_pipe": exp_pipe, "mma_rate": mma_rate, "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": args.steps,  # one prefill kernel per timed step
             "gpu": torch.cuda.get_device_name(device),

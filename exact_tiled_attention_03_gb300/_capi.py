@@ -52,6 +52,7 @@ SIGNATURES = {
     "fa_selftest_umma_f8": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_wait_timeout": (_I32, [_U64, _P]),
     "fa_selftest_mufu": (_I32, [_P, _I32, _I32, _P]),
+    "fa_selftest_mma_rate": (_I32, [_P, _I32, _I32, _I32, _P]),
 }
 
 _lib = None
@@ -226,6 +227,11 @@ def fa_selftest_umma_f8(a, b, c, n, b_mn_major, a_tmem, stream=None) -> int:
 
 def fa_selftest_mufu(out, blocks, iters, stream=None) -> int:
     return load().fa_selftest_mufu(_ptr(out), int(blocks), int(iters), _stream(stream))
+
+
+def fa_selftest_mma_rate(cycles, mode, blocks, iters, stream=None) -> int:
+    return load().fa_selftest_mma_rate(_ptr(cycles), int(mode), int(blocks), int(iters),
+                                       _stream(stream))
 
 
 def fa_selftest_wait_timeout(timeout_ns, stream=None) -> int:

@@ -749,6 +749,22 @@ fa_status_t fa_selftest_mufu(float *out, int blocks, int iters, void *stream)
     return launch_selftest_mufu(out, blocks, iters, static_cast<cudaStream_t>(stream));
 }
 
+fa_status_t fa_selftest_mma_rate(long long *cycles, int mode, int blocks, int iters, void *stream)
+{
+    if (!cycles || blocks <= 0 || iters <= 0)
+        return FA_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 4)
+        return FA_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(cycles) % alignof(long long) != 0)
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_mma_rate(cycles, mode, blocks, iters, static_cast<cudaStream_t>(stream),
+                                    di->status);
+}
+
 fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
 {
     if (timeout_ns == 0 || timeout_ns > 10000000000ull)

@@ -27,9 +27,9 @@
 //     lands, written back as bf16 over dP's columns, and dQ += dS K_j (A
 //     from TMEM). Issue order S(j+1) | dQ(j) dP(j+1) S(j+2) | ..., with K
 //     in a 3-deep ring of its own (K_j is read by S(j) and again by dQ(j)).
-// All score MMAs are 128 wide: an M = 128 MMA of N = 64 columns takes 54
-// cycles against 64 for N = 128 (K = 16, measured), so two 64-wide halves
-// take 1.7x the tensor time of one 128-wide MMA.
+// All score MMAs are 128 wide: an M = 128 MMA of N = 64 columns takes 45 to
+// 54 cycles against 64 for N = 128 (K = 16, measured), so two 64-wide halves
+// take 1.4x to 1.7x the tensor time of one 128-wide MMA.
 // The math warps are 8: the two warps of a sub-partition share TMEM lanes
 // (lane quarter = warp mod 4) and split the columns; each packs its bf16
 // result into the first 32 of its 64 columns (0-31 and 64-95 of a region),

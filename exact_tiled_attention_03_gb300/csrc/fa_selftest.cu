@@ -9,6 +9,9 @@
 //  * fa_selftest_umma_f8_kernel: the E4M3 products of the FP8 forward (A from
 //    shared or tensor memory, B K-major or MN-major).
 //  * fa_selftest_mufu_kernel: exp2 (MUFU) throughput, the softmax's second bound.
+//  * fa_selftest_mma_rate_kernel: cycles per bf16 tcgen05.mma for the operand
+//    shapes the kernels choose between (N = 64 / 128 / 256, A from shared or
+//    tensor memory).
 //  * fa_selftest_wait_kernel: the bounded mbarrier wait of the attention
 //    kernels on a barrier that nothing completes; it must give up after the
 //    limit, set the device status word and return.
@@ -304,6 +307,104 @@ __global__ void __launch_bounds__(256) fa_selftest_mufu_kernel(float *out, int i
     out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// Cycles the tensor core takes per 128 x 128 x 128 bf16 product (8
+// instructions of K = 16) in operand form `mode`:
+//   0: A and B from shared memory, N = 128;   1: the same as two N = 64 halves;
+//   2: A from tensor memory, N = 128;         3: the same as two N = 64 halves;
+//   4: A and B from shared memory, N = 256 (two products per 8 instructions).
+// A half is 8 back-to-back MMAs into one accumulator, as a kernel that splits
+// its score tile into column halves issues them.
+// One thread per CTA issues `iters` rounds back to back and records the
+// clock64 difference from before the first issue to the completion of the
+// last (one commit). Operand values are a constant bf16 pattern; the
+// accumulator is overwritten at each round's first K step.
+__global__ void __launch_bounds__(128, 1)
+    fa_selftest_mma_rate_kernel(int mode, int iters, long long *cycles, unsigned int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    constexpr int kOffA = 0, kOffB = 32768, kOffBar = 32768 + 65536;  // A 128 x 128, B 256 x 128
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(smem + kOffBar + 64);
+    for (int i = threadIdx.x; i < kOffBar / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t *>(smem)[i] = 0x3C003C00u;  // bf16 2^-7 pairs
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_base;
+    if (threadIdx.x == 0) {
+        const uint64_t a0 = smem_desc_sw128(smem_u32(smem + kOffA), 16, 1024);
+        const uint64_t b0 = smem_desc_sw128(smem_u32(smem + kOffB), 16, 1024);
+        constexpr uint32_t i128 = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t i64 = idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t i256 = idesc_bf16_f32(128, 256, false, false);
+        // K-major boxes of 64 columns: 16 KB per box for 128 rows, 32 KB for 256
+        auto koff = [](int kk, int box) -> uint64_t {
+            return static_cast<uint64_t>(((kk / 4) * box + (kk % 4) * 32) >> 4);
+        };
+        // columns 0-63 of tensor memory hold the A operand of the TS forms
+        for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ss(tmem, a0 + koff(kk, 16384), b0 + koff(kk, 16384), i128, kk > 0);
+        umma_commit(bar);
+        bool ok = mbar_wait_drain(bar, 0, status);
+        tc_fence_after_sync();
+        // One loop per form, so that nothing but the MMAs sits in the issue loop.
+        const long long t0 = clock64();
+        if (ok && mode == 0) {
+            for (int it = 0; it < iters; ++it)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ss(tmem + 256, a0 + koff(kk, 16384), b0 + koff(kk, 16384), i128,
+                                 kk > 0);
+        } else if (ok && mode == 1) {
+            for (int it = 0; it < iters; ++it)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16_ss(tmem + 256 + 64 * h, a0 + koff(kk, 16384),
+                                     b0 + koff(kk, 16384) + ((8192 * h) >> 4), i64, kk > 0);
+        } else if (ok && mode == 2) {
+            for (int it = 0; it < iters; ++it)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ts(tmem + 256, tmem + kk * 8, b0 + koff(kk, 16384), i128, kk > 0);
+        } else if (ok && mode == 3) {
+            for (int it = 0; it < iters; ++it)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16_ts(tmem + 256 + 64 * h, tmem + kk * 8,
+                                     b0 + koff(kk, 16384) + ((8192 * h) >> 4), i64, kk > 0);
+        } else if (ok) {
+            for (int it = 0; it < iters; ++it)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ss(tmem + 256, a0 + koff(kk, 16384), b0 + koff(kk, 32768), i256,
+                                 kk > 0);
+        }
+        umma_commit(bar);
+        ok = ok && mbar_wait_drain(bar, 1, status);
+        cycles[blockIdx.x] = ok ? clock64() - t0 : -1;
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (threadIdx.x < 32)
+        tmem_dealloc(tmem, 512);
+}
+
 __global__ void fa_selftest_wait_kernel(uint64_t limit_ns, unsigned int *status)
 {
     __shared__ uint64_t bar;
@@ -383,6 +484,18 @@ fa_status_t launch_selftest_umma_f8(const void *a, const void *b, float *c, int 
 fa_status_t launch_selftest_mufu(float *out, int blocks, int iters, cudaStream_t stream)
 {
     selftest::fa_selftest_mufu_kernel<<<blocks, 256, 0, stream>>>(out, iters);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t launch_selftest_mma_rate(long long *cycles, int mode, int blocks, int iters,
+                                     cudaStream_t stream, unsigned int *status)
+{
+    const int smem = 32768 + 65536 + 128 + 1024;
+    if (cudaFuncSetAttribute(selftest::fa_selftest_mma_rate_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return FA_ERR_CUDA;
+    selftest::fa_selftest_mma_rate_kernel<<<blocks, 128, smem, stream>>>(mode, iters, cycles,
+                                                                        status);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

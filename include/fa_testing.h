@@ -69,6 +69,26 @@ fa_status_t fa_selftest_umma_f8(const void *a, const void *b, float *c, int n, i
 fa_status_t fa_selftest_mufu(float *out, int blocks, int iters, void *stream);
 
 /*
+ * tcgen05.mma rate microbenchmark (bf16 operands, fp32 accumulator, M = 128):
+ * `blocks` CTAs (one per SM at most is meaningful; each holds 97 KB of shared
+ * memory and all 512 TMEM columns), one thread each issuing `iters` rounds of
+ * one 128 x 128 x 128 product as 8 instructions of K = 16, in form `mode`:
+ *   0  A and B from shared memory, N = 128
+ *   1  A and B from shared memory, two N = 64 halves (each 8 back-to-back
+ *      MMAs into its own accumulator)
+ *   2  A from tensor memory, N = 128
+ *   3  A from tensor memory, two N = 64 halves
+ *   4  A and B from shared memory, N = 256 (a round is two products)
+ * cycles[b] (device memory, `blocks` entries) receives the SM clock cycles of
+ * CTA b from its first issue to the completion of its last MMA, or -1 if the
+ * bounded wait for completion gave up (the device status word then records
+ * the timeout). Used to choose the MMA shapes of the gradient kernels.
+ * Returns FA_ERR_UNSUPPORTED for another mode, FA_ERR_INVALID_ARG for a null
+ * pointer or a non-positive count.
+ */
+fa_status_t fa_selftest_mma_rate(long long *cycles, int mode, int blocks, int iters, void *stream);
+
+/*
  * Launches one CTA whose thread waits, with the same bounded wait the
  * attention kernels use, on an mbarrier that nothing ever completes. After
  * `timeout_ns` nanoseconds the wait gives up and sets the device status word

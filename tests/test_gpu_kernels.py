@@ -71,6 +71,29 @@ def test_mufu_microbenchmark_runs():
     assert ((v / 8 + 0.59).abs() < 0.02).all()
 
 
+def test_mma_rate_of_the_operand_forms():
+    """The gradient kernels issue only 128-wide MMAs because two 64-wide halves
+    take longer than one 128-wide MMA of the same work (measured 45-54 against 64
+    cycles per K = 16 instruction). Cycle counts do not depend on the clock."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc = torch.empty(sms, dtype=torch.int64, device="cuda")
+    per = {}
+    for mode in range(5):
+        for _ in range(2):  # the first launch of a form warms the tensor pipe up
+            _capi.check(_capi.fa_selftest_mma_rate(cyc, mode, sms, 1000), "mma_rate")
+        torch.cuda.synchronize()
+        c = cyc.cpu()
+        assert (c > 0).all()
+        per[mode] = c.double().median().item() / (1000 * (2 if mode == 4 else 1))
+    assert _capi.fa_device_status() == _capi.FA_OK
+    for mode in (0, 2, 4):          # full-width forms run near the nominal 512
+        assert 480 < per[mode] < 620, per
+    for half, full in ((1, 0), (3, 2)):
+        assert per[half] > 1.25 * per[full], per
+    assert _capi.fa_selftest_mma_rate(cyc, 5, 1, 1) == _capi.FA_ERR_UNSUPPORTED
+    assert _capi.fa_selftest_mma_rate(None, 0, 1, 1) == _capi.FA_ERR_INVALID_ARG
+
+
 def test_bounded_wait_reports_a_timeout_without_faulting():
     """A wait on a barrier nothing completes gives up, sets the status word, returns."""
     assert _capi.fa_device_status() == _capi.FA_OK
