@@ -351,6 +351,40 @@ def measure_backward(w, device, sptr, args, peaks):
                         for k in ("fa_bwd_dkdv_kernel<128>", "fa_bwd_dq_kernel<128>")}}
 
 
+OTHER_FORWARD = ("prefill_b4h32s2048d128_causal", "prefill_b4h32s2048d128_causal_q4",
+                 "prefill_b1h32s32768d64_causal")
+
+
+def measure_other_forward(device, sptr, args, peaks):
+    """The other prefill configurations (2K, 2K with Q x 4, 32K at d = 64) through the
+    same entry point, each against the bf16 tensor roofline."""
+    from exact_tiled_attention_03_gb300 import _capi
+
+    out = {}
+    for name in OTHER_FORWARD:
+        w = WORKLOADS[name]
+        q, k, v = (t.to(device) for t in make_qkv(w))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=device)
+
+        def step():
+            st = _capi.fa_forward(q, k, v, o, lse, w.B, w.H, w.Sq, w.Sk, w.d, w.causal, w.scale,
+                                  sptr)
+            if st != 0:
+                raise _capi.FAError(st, "fa_forward")
+
+        for _ in range(args.warmup):
+            step()
+        n = max(10, min(200, int(0.2 / max(1e-6, w.exact_flops() / 1e15))))
+        per = time_steps(step, n, torch.cuda.current_stream(device)) / n
+        _capi.check(_capi.fa_device_status(sptr), "device status after " + name)
+        tf = w.exact_flops() / per / 1e12
+        out[name] = {"ms_per_step": per * 1e3, "TFLOP/s": tf,
+                     "frac_bf16_peak": tf / peaks["bf16_tflops"], "steps": n}
+        del q, k, v, o, lse
+    return out
+
+
 def measure_fp8(w, device, sptr, args, peaks):
     """The FP8 forward (E4M3 Q, K, V with per-tensor descales, bf16 O) on the same
     workload and algorithmic FLOPs, against the FP8 dense peak: the measured
@@ -563,6 +597,9 @@ def run_ours(args, world, rank, local):
     if not args.no_fp8:
         fp8 = measure_fp8(w, device, sptr, args, peaks)
 
+    # the other prefill configurations
+    forward_other = measure_other_forward(device, sptr, args, peaks)
+
     # the exp-pipe bound of the prefill step (MUFU microbenchmark)
     exp_pipe = measure_exp_pipe(w, device, sptr)
     mma_rate = measure_mma_rate(device, sptr)
@@ -607,7 +644,8 @@ def run_ours(args, world, rank, local):
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
             "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "backward": backward,
-            "fp8": fp8, "exp_pipe": exp_pipe, "mma_rate": mma_rate, "cpu_baseline": cpu,
+            "fp8": fp8, "forward_other": forward_other, "exp_pipe": exp_pipe, "mma_rate": mma_rate,
+            "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": args.steps,  # one prefill kernel per timed step
             "gpu": torch.cuda.get_device_name(device),
