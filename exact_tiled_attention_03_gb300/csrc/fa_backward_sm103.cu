@@ -30,10 +30,11 @@
 // All score MMAs are 128 wide: an M = 128 MMA of N = 64 columns takes 45 to
 // 54 cycles against 64 for N = 128 (K = 16, measured), so two 64-wide halves
 // take 1.4x to 1.7x the tensor time of one 128-wide MMA.
-// The math warps are 8: the two warps of a sub-partition share TMEM lanes
-// (lane quarter = warp mod 4) and split the columns; each packs its bf16
-// result into the first 32 of its 64 columns (0-31 and 64-95 of a region),
-// so neither overwrites columns the other has yet to read.
+// Math warps share TMEM lanes by sub-partition (lane quarter = warp mod 4)
+// and split the columns: 16 warps of 32 columns in the dK/dV kernel, whose
+// P^T rebuild is on the MMA chain, 8 warps of 64 in the dQ kernel. Each
+// packs its bf16 result into the first half of its own columns, so no warp
+// overwrites columns another has yet to read.
 // The dQ kernel is launched with programmatic stream serialization: its CTAs
 // start on the SMs the dK/dV kernel's last CTAs leave idle (it reads only
 // what the prep kernel wrote), and wait for the dK/dV grid before exiting, so
@@ -49,10 +50,19 @@ namespace fa {
 namespace bwd {
 
 constexpr int kBlock = 128;             // keys or queries per tile = TMEM lanes
-constexpr int kMathThreads = 256;       // warps 0-7: lane quarter warp % 4, column half warp / 4
-constexpr int kThreads = kMathThreads + 64;  // + warp 8 producer, warp 9 MMA
+// dQ kernel: warps 0-7 do the math (lane quarter warp % 4, column half
+// warp / 4), warp 8 loads, warp 9 issues the MMAs.
+constexpr int kMathThreads = 256;
+constexpr int kThreads = kMathThreads + 64;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// dK/dV kernel: warps 0-15 do the math (lane quarter warp % 4, column
+// quarter warp / 4: 32 columns each), warp 16 loads, warp 17 issues.
+constexpr int kKvGroups = 4;
+constexpr int kKvMathThreads = kKvGroups * 128;
+constexpr int kKvThreads = kKvMathThreads + 64;
+constexpr int kKvProducerWarp = kKvMathThreads / 32;
+constexpr int kKvMmaWarp = kKvProducerWarp + 1;
 constexpr int kHalf = kBlock / 2;        // score columns per half
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = kBlock * 128;  // 128 rows x 64 columns bf16
@@ -207,47 +217,68 @@ __device__ __forceinline__ void rebuild_ds(const uint32_t (&dt)[32], const float
     }
 }
 
+// 16 TMEM columns of this thread's lane, with the wait.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // The epilogue of both gradient kernels: a 128 x D fp32 tile in TMEM (this
 // thread's lane = row r; `taddr` addresses column 0 of that lane) times
 // `mul`, to bf16, through shared memory (Q-tile sized staging at `stage`,
-// swizzled like the TMA box), then TMA-stored. Column half `half` of the
-// tile is this thread's; all math threads take part.
-template <int D>
+// swizzled like the TMA box), then TMA-stored. The tile's columns are split
+// into kGroups groups; group `group` is this thread's. All kGroups * 128
+// math threads take part.
+template <int D, int kGroups>
 __device__ __forceinline__ void store_tile(uint32_t taddr, float mul, bool have, uint8_t *stage,
                                            const CUtensorMap *map, int row0, int bh, int r,
-                                           int half, uint32_t bar_id)
+                                           int group, uint32_t bar_id)
 {
+    constexpr int kCols = D / kGroups;
+    constexpr int kStep = kCols < 32 ? kCols : 32;
+    static_assert(kStep == 16 || kStep == 32, "16 or 32 columns per load");
     const uint32_t st_a = smem_u32(stage);
 #pragma unroll
-    for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
-        uint32_t v[32];
+    for (int c0 = group * kCols; c0 < (group + 1) * kCols; c0 += kStep) {
+        uint32_t v[kStep];
         if (have) {
-            tmem_ld32_wait(taddr + c0, v);
+            if constexpr (kStep == 32)
+                tmem_ld32_wait(taddr + c0, v);
+            else
+                tmem_ld16_wait(taddr + c0, v);
         } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
+            for (int c = 0; c < kStep; ++c)
                 v[c] = 0u;
         }
-        uint32_t pk[16];
+        uint32_t pk[kStep / 2];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
+        for (int c = 0; c < kStep; c += 2)
             pk[c / 2] = pk2(__uint_as_float(v[c]) * mul, __uint_as_float(v[c + 1]) * mul);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kStep / 8; ++q) {
             const uint32_t chunk = ((c0 % 64) / 8) + q;
             st_shared_v4(st_a + (c0 / 64) * kBoxBytes + sw128_offset(static_cast<uint32_t>(r), chunk),
                          pk[q * 4], pk[q * 4 + 1], pk[q * 4 + 2], pk[q * 4 + 3]);
         }
     }
     fence_proxy_async_smem();
-    named_bar_sync(bar_id, kMathThreads);
-    if (r == 0 && half == 0) {
+    named_bar_sync(bar_id, kGroups * 128);
+    if (r == 0 && group == 0) {
         for (int b = 0; b < D / 64; ++b)
             tma_store_3d(map, stage + b * kBoxBytes, b * 64, row0, bh);
         tma_store_commit();
         tma_store_wait_read_all();
     }
-    named_bar_sync(bar_id, kMathThreads);
+    named_bar_sync(bar_id, kGroups * 128);
 }
 
 // ---------------------------------------------------------------- dK, dV
@@ -276,7 +307,7 @@ struct KvBars {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -312,14 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->dp_full, 1);
-        mbar_init(&bars->p_full, kMathThreads / 32);
-        mbar_init(&bars->ds_full, kMathThreads / 32);
+        mbar_init(&bars->p_full, kKvMathThreads / 32);
+        mbar_init(&bars->ds_full, kKvMathThreads / 32);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kKvMmaWarp) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -329,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
     int *abort_flag = &bars->abort_flag;
 
-    if (warp == kProducerWarp) {
+    if (warp == kKvProducerWarp) {
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTile);
             for (int b = 0; b < D / 64; ++b) {
@@ -357,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = max(0, n - C::kStages); k < n; ++k)
                 mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kKvMmaWarp) {
         if (lane == 0 && n_q > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlock, kBlock, false, false);
             constexpr uint32_t idesc_g = idesc_bf16_f32(kBlock, D, false, true);
@@ -379,9 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(dp ? &bars->dp_full : &bars->s_full);
             };
             // dV += P^T dO (A = P^T from the S columns) or dK += dS^T Q (A =
-            // dS^T from the dP columns). A is bf16 pairs: queries 0-63 in the
-            // region's columns 0-31, queries 64-127 in columns 64-95. B (dO,
-            // Q) MN-major from shared memory.
+            // dS^T from the dP columns). A is bf16 pairs, each 32-query group
+            // packed into its first 16 columns: K step kk (queries 16 kk ..
+            // 16 kk + 15) at column (kk / 2) * 32 + (kk % 2) * 8. B (dO, Q)
+            // MN-major from shared memory.
             auto issue_grad = [&](int n, bool dk) {
                 const uint32_t sq = ring + (n % C::kStages) * C::kStageBytes + (dk ? 0 : C::kTile);
                 const uint64_t b0 = smem_desc_sw128(sq, kBoxBytes, 1024);
@@ -389,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kBlock / 16; ++kk)
                     umma_bf16_ts(tmem + (dk ? C::kColDK : C::kColDV),
-                                 a0 + (kk / 4) * kHalf + (kk % 4) * 8,
+                                 a0 + (kk / 2) * kChunk + (kk % 2) * 8,
                                  b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (n > 0 || kk > 0) ? 1u : 0u);
             };
@@ -436,51 +468,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ math warps
-        const int quarter = warp & 3, half = warp >> 2;
+        // 16 warps: lane quarter warp % 4 (key rows), column quarter warp / 4
+        // (queries 32 cq .. 32 cq + 31 of the tile); each packs its bf16
+        // result into the first 16 of its own 32 columns.
+        const int quarter = warp & 3, cq = warp >> 2;
         const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane
         const int key = kv0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS + half * kHalf;
-        const uint32_t tDP = tmem + lane_base + C::kColDP + half * kHalf;
+        const uint32_t tS = tmem + lane_base + C::kColS + cq * kChunk;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + cq * kChunk;
         const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
+        const bool in_k = key < p.Sk;
         bool ok = true;
         for (int n = 0; n < n_q && ok; ++n) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, n & 1, abort_flag, p.status));
             if (!ok)
                 break;
             tc_fence_after_sync();
-            const int q0 = (qt0 + n) * kBlock + half * kHalf;  // first query of this half
+            const int q0 = (qt0 + n) * kBlock + cq * kChunk;  // first query of this thread's columns
             const float *vec = reinterpret_cast<const float *>(smem + C::kOffVec +
                                                                (n % C::kStages) * 1024) +
-                               half * kHalf;
+                               cq * kChunk;
             // mask: key beyond Sk, or (causal) key after the query's last visible key
-            const bool tile_masked = key >= p.Sk || (p.causal && kv0 + kBlock - 1 > q0 + off);
-            // P^T = 2^(S^T sl2 - lse2) for this thread's 64 queries, kept in
-            // fp32 for dS^T. Chunk 1's loads are in flight while chunk 0 is
-            // rebuilt.
-            float pv[kHalf];
+            const bool masked = !in_k || (p.causal && kv0 + kBlock - 1 > q0 + off);
+            // P^T = 2^(S^T sl2 - lse2), kept in fp32 for dS^T
+            float pv[kChunk];
             {
-                uint32_t sd[2][kChunk];
-                tmem_ld32_wait(tS, sd[0]);
-                tmem_ld32_nowait(tS + kChunk, sd[1]);
-#pragma unroll
-                for (int ch = 0; ch < kHalf / kChunk; ++ch) {
-                    const int c0 = ch * kChunk;
-                    if (ch > 0)
-                        tmem_ld_wait_regs32(sd[ch]);
-                    uint32_t pp[kChunk / 2];
-                    if (!tile_masked) {
-                        rebuild_p<false>(sd[ch], sl2x2, vec + c0, [](int) { return true; },
-                                         pv + c0, pp);
-                    } else {
-                        const int lim = q0 + c0 + off;  // query of column c sees key <= lim + c
-                        const bool in_k = key < p.Sk;
-                        rebuild_p<true>(sd[ch], sl2x2, vec + c0,
-                                        [&](int c) { return in_k && (!p.causal || key <= lim + c); },
-                                        pv + c0, pp);
-                    }
-                    tmem_st16(tS + c0 / 2, pp);  // over this half's own, already read columns
+                uint32_t sd[kChunk];
+                tmem_ld32_wait(tS, sd);
+                uint32_t pp[kChunk / 2];
+                if (!masked) {
+                    rebuild_p<false>(sd, sl2x2, vec, [](int) { return true; }, pv, pp);
+                } else {
+                    const int lim = q0 + off;  // the query of column c sees key <= lim + c
+                    rebuild_p<true>(sd, sl2x2, vec,
+                                    [&](int c) { return in_k && (!p.causal || key <= lim + c); },
+                                    pv, pp);
                 }
+                tmem_st16(tS, pp);  // over this thread's own, already read columns
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -493,18 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             // dS^T = P^T (dP^T - D)
             {
-                uint32_t sd[2][kChunk];
-                tmem_ld32_wait(tDP, sd[0]);
-                tmem_ld32_nowait(tDP + kChunk, sd[1]);
-#pragma unroll
-                for (int ch = 0; ch < kHalf / kChunk; ++ch) {
-                    const int c0 = ch * kChunk;
-                    if (ch > 0)
-                        tmem_ld_wait_regs32(sd[ch]);
-                    uint32_t pd[kChunk / 2];
-                    rebuild_ds(sd[ch], pv + c0, vec + 128 + c0, pd);
-                    tmem_st16(tDP + c0 / 2, pd);
-                }
+                uint32_t sd[kChunk];
+                tmem_ld32_wait(tDP, sd);
+                uint32_t pd[kChunk / 2];
+                rebuild_ds(sd, pv, vec + 128, pd);
+                tmem_st16(tDP, pd);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -518,14 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
         }
         // All math threads take the epilogue (and its barriers) or none does.
+        const uint32_t lane_tm = tmem + lane_base;
         const bool skip =
-            named_bar_or(1, kMathThreads, !ok || *reinterpret_cast<volatile int *>(abort_flag));
+            named_bar_or(1, kKvMathThreads, !ok || *reinterpret_cast<volatile int *>(abort_flag));
         if (!skip) {
             uint8_t *stage = smem + C::kOffRing;  // the ring is idle now
-            store_tile<D>(tmem + lane_base + C::kColDV, 1.0f, n_q > 0, stage, &tm_dv, kv0, bh, r,
-                          half, 2);
-            store_tile<D>(tmem + lane_base + C::kColDK, p.scale, n_q > 0, stage, &tm_dk, kv0, bh,
-                          r, half, 2);
+            store_tile<D, kKvGroups>(lane_tm + C::kColDV, 1.0f, n_q > 0, stage, &tm_dv, kv0, bh, r,
+                                     cq, 2);
+            store_tile<D, kKvGroups>(lane_tm + C::kColDK, p.scale, n_q > 0, stage, &tm_dk, kv0,
+                                     bh, r, cq, 2);
         }
     }
     // Threads that issued TMA stores wait for their writes (not only for the
@@ -535,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (warp == kMmaWarp)
+    if (warp == kKvMmaWarp)
         tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -859,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool skip =
             named_bar_or(1, kMathThreads, !ok || *reinterpret_cast<volatile int *>(abort_flag));
         if (!skip)
-            store_tile<D>(tmem + lane_base + C::kColDQ, p.scale, n_kv > 0, smem + C::kOffQ,
+            store_tile<D, 2>(tmem + lane_base + C::kColDQ, p.scale, n_kv > 0, smem + C::kOffQ,
                           &tm_dq, q0, bh, r, half, 2);
     }
     // Threads that issued TMA stores wait for their writes (not only for the
@@ -922,7 +941,7 @@ fa_status_t launch(const BackwardProblem &bp)
         const uint64_t grid = static_cast<uint64_t>(p.n_ktiles) * BH;
         if (grid > 0x7FFFFFFFull)
             return FA_ERR_UNSUPPORTED;
-        kern<<<static_cast<unsigned>(grid), kThreads, KvCfg<D>::kSmem, pr.stream>>>(tq, tk, tv, tdo,
+        kern<<<static_cast<unsigned>(grid), kKvThreads, KvCfg<D>::kSmem, pr.stream>>>(tq, tk, tv, tdo,
                                                                                    tdk, tdv, p);
         if (cudaGetLastError() != cudaSuccess)
             return FA_ERR_CUDA;
