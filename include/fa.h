@@ -243,11 +243,16 @@ fa_status_t fa_verify_paged_forward(const void *q, const void *k_pages, const vo
  *   q, k, v, o, lse, causal, scale : as passed to / returned by fa_forward.
  *   dout      : device bf16 [B, H, Sq, d].
  *   dq        : device bf16 [B, H, Sq, d];  dk, dv: device bf16 [B, H, Sk, d].
- *   workspace : fa_backward_workspace_size() bytes of device memory (D and
- *               LSE per padded query row), 256-byte aligned; NULL takes it
- *               from the stream-ordered allocator on `stream`.
- * Rows with no visible key contribute nothing. Same shape limits and errors
- * as fa_prefill_forward.
+ *   workspace : fa_backward_workspace_size() bytes of device memory
+ *               (scratch: -D and -LSE * log2(e) per padded query row),
+ *               256-byte aligned; NULL takes it from the stream-ordered
+ *               allocator on `stream`.
+ * Enqueues three kernels on `stream`. The third (dQ) is launched with
+ * programmatic stream serialization so that it starts on the SMs the second
+ * (dK, dV) leaves idle; it waits for the second before completing, so the
+ * call as a whole is ordered on `stream` like any other (also under CUDA
+ * graph capture). Rows with no visible key contribute nothing. Same shape
+ * limits and errors as fa_prefill_forward.
  */
 fa_status_t fa_backward(const void *q, const void *k, const void *v, const void *o,
                         const float *lse, const void *dout, void *dq, void *dk, void *dv,
