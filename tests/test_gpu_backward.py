@@ -141,3 +141,44 @@ def test_backward_is_deterministic():
     b = run_fwd_bwd(q, k, v, do, True, w.scale)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_backward_cuda_graph_replay():
+    """The backward (three kernels, the last launched with programmatic stream
+    serialization) captured in a CUDA graph and replayed on new inputs gives the
+    bits an eager call gives, and the graph's completion orders a dependent copy."""
+    w = custom(1, 2, 640, 640, 128, True, seed=31, q_factor=2.0)
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    do = upstream(q.cpu(), 32).cuda()
+    B, H, Sq, Sk, d = w.B, w.H, w.Sq, w.Sk, w.d
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nb = _capi.fa_backward_workspace_size(B, H, Sq, Sk, d)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def fwd_bwd(stream):
+        _capi.check(_capi.fa_prefill_forward(q, k, v, o, lse, B, H, Sq, Sk, d, True, w.scale,
+                                             stream), "fwd")
+        _capi.check(_capi.fa_backward(q, k, v, o, lse, do, dq, dk, dv, B, H, Sq, Sk, d, True,
+                                      w.scale, ws, nb, stream), "bwd")
+
+    with torch.cuda.stream(s):  # warm-up (kernel attributes) before capture
+        fwd_bwd(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fwd_bwd(s)
+        dk_copy = dk.clone()  # ordered after the whole backward
+    for seed in (33, 34):
+        qn, kn, vn = make_qkv(custom(B, H, Sq, Sk, d, True, seed=seed, q_factor=2.0))
+        q.copy_(qn); k.copy_(kn); v.copy_(vn)
+        g.replay()
+        torch.cuda.synchronize()
+        got = (dq.clone(), dk.clone(), dv.clone(), dk_copy.clone())
+        with torch.cuda.stream(s):
+            fwd_bwd(s)
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], dq) and torch.equal(got[1], dk) and torch.equal(got[2], dv)
+        assert torch.equal(got[3], dk)
