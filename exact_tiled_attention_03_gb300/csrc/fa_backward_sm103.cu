@@ -97,32 +97,42 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 }
 
 // ---------------------------------------------------------------- prep
-// One warp per (bh, row of the padded row range).
+// D / 8 threads per (bh, row of the padded row range), each reading 16 bytes
+// of O and of dO.
 template <int D>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                        const float *__restrict__ lse, float *__restrict__ lse2,
                        float *__restrict__ Dvec, int BH, int Sq, int Sq_pad)
 {
-    const int row = blockIdx.x * 8 + threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    if (row >= BH * Sq_pad)
+    constexpr int kLanes = D / 8;  // threads per row
+    const int row = blockIdx.x * (256 / kLanes) + threadIdx.x / kLanes;
+    const int part = threadIdx.x % kLanes;
+    if (row >= BH * Sq_pad)  // whole row groups: the shuffles below stay within live lanes
         return;
     const int bh = row / Sq_pad, i = row % Sq_pad;
     float acc = 0.0f;
     float l2 = INFINITY;
     if (i < Sq) {
-        const size_t base = (static_cast<size_t>(bh) * Sq + i) * D;
+        const size_t base = (static_cast<size_t>(bh) * Sq + i) * D + part * 8;
+        const uint4 ov = *reinterpret_cast<const uint4 *>(o + base);
+        const uint4 dv = *reinterpret_cast<const uint4 *>(dout + base);
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-        for (int t = lane; t < D; t += 32)
-            acc = fmaf(__bfloat162float(o[base + t]), __bfloat162float(dout[base + t]), acc);
+        for (int e = 0; e < 4; ++e) {
+            const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[e]));
+            const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&dw[e]));
+            acc = fmaf(of.x, df.x, acc);
+            acc = fmaf(of.y, df.y, acc);
+        }
         const float L = lse[static_cast<size_t>(bh) * Sq + i];
         l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
     }
+    const unsigned mask = __activemask();
 #pragma unroll
-    for (int off = 16; off > 0; off /= 2)
-        acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {  // stored negated: the rebuilds add them
+    for (int off = kLanes / 2; off > 0; off /= 2)
+        acc += __shfl_xor_sync(mask, acc, off);
+    if (part == 0) {  // stored negated: the rebuilds add them
         Dvec[row] = -acc;
         lse2[row] = -l2;
     }
@@ -905,7 +915,8 @@ fa_status_t launch(const BackwardProblem &bp)
     float *Dvec = lse2 + static_cast<size_t>(BH) * Sq_pad;
     {
         const int rows = static_cast<int>(BH * Sq_pad);
-        fa_bwd_prep_kernel<D><<<(rows + 7) / 8, 256, 0, pr.stream>>>(
+        constexpr int kRowsPerBlock = 256 / (D / 8);
+        fa_bwd_prep_kernel<D><<<(rows + kRowsPerBlock - 1) / kRowsPerBlock, 256, 0, pr.stream>>>(
             static_cast<const __nv_bfloat16 *>(bp.o), static_cast<const __nv_bfloat16 *>(bp.dout),
             bp.lse, lse2, Dvec, static_cast<int>(BH), static_cast<int>(pr.Sq), Sq_pad);
         if (cudaGetLastError() != cudaSuccess)
