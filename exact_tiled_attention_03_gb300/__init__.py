@@ -9,14 +9,16 @@ current stream.
 from __future__ import annotations
 
 from ._capi import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED,
-                    FA_ERR_WORKSPACE, FA_OK, FA_VERIFY_MAX_SQ, FAError, check, fa_device_status,
+                    FA_ERR_WORKSPACE, FA_OK, FA_VERIFY_MAX_SQ, FAError, check, fa_backward,
+                    fa_backward_workspace_size, fa_device_status,
                     fa_forward, fa_forward_fp8, fa_forward_ws, fa_prefill_forward,
                     fa_status_string,
                     fa_verify_auto_splits, fa_verify_forward, fa_verify_workspace_size,
                     fa_workspace_size, load)
 
 __all__ = [
-    "attention", "attention_fp8", "fa_forward", "fa_forward_fp8", "fa_forward_ws", "fa_prefill_forward", "fa_verify_forward",
+    "attention", "attention_fp8", "attention_backward", "fa_backward",
+    "fa_backward_workspace_size", "fa_forward", "fa_forward_fp8", "fa_forward_ws", "fa_prefill_forward", "fa_verify_forward",
     "fa_workspace_size", "fa_verify_workspace_size", "fa_verify_auto_splits", "fa_status_string",
     "fa_device_status", "FAError", "check", "load", "FA_OK", "FA_ERR_INVALID_ARG",
     "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE", "FA_VERIFY_MAX_SQ",
@@ -71,3 +73,28 @@ def attention_fp8(q8, k8, v8, causal: bool = False, scale: float | None = None,
     check(fa_forward_fp8(q8, k8, v8, o, lse, B, H, Sq, Sk, d, causal, scale, descale[0],
                          descale[1], descale[2], stream), "fa_forward_fp8")
     return o, lse
+
+
+def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
+                       stream=None):
+    """dQ, dK, dV of O = attention(Q, K, V) given the forward's O and LSE and the
+    upstream gradient dO (contiguous bf16 CUDA tensors [B, H, S, d]; LSE fp32
+    [B, H, Sq] as ``attention`` returns it); runs ``fa_backward`` with a
+    workspace from the stream-ordered allocator. Raises FAError on a non-OK
+    status.
+    """
+    import math
+
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor [B, H, S, d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    check(fa_backward(q, k, v, o, lse, do, dq, dk, dv, B, H, Sq, Sk, d, causal, scale, None, 0,
+                      stream), "fa_backward")
+    return dq, dk, dv
