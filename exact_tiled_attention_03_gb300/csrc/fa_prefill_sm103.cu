@@ -504,16 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // P (bf16 pairs) over S_t's first 64 columns, then publish.
-                {
-                    uint32_t lo[32], hi[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        lo[c] = pk[c];
-                        hi[c] = pk[32 + c];
-                    }
-                    tmem_st32(tS, lo);
-                    tmem_st32(tS + 32, hi);
-                }
+                tmem_st64(tS, pk);
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
