@@ -251,6 +251,21 @@ bool encode_tmap_u8_3d(CUtensorMap *map, const void *base, uint64_t inner, uint6
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_bf16_pages_5d(CUtensorMap *map, const void *base, uint64_t page_size, uint64_t H,
+                               uint64_t num_pages)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[5] = {64, 2, page_size, H, num_pages};
+    const cuuint64_t strides[4] = {128, 256, page_size * 256, H * page_size * 256};
+    const cuuint32_t box[5] = {64, 2, static_cast<cuuint32_t>(page_size), 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                          uint64_t mid, uint64_t outer, uint32_t box_rows)
 {

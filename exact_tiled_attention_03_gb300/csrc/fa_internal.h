@@ -40,6 +40,11 @@ bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uin
 bool encode_tmap_u8_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                        uint64_t depth, uint32_t box_rows);
 
+// Pages [num_pages, H, page_size, 128] bf16 as (64 columns, 2 column halves,
+// page_size rows, H, num_pages), box = one page of one head (page_size * 256
+// bytes), 128-byte swizzle.
+bool encode_tmap_bf16_pages_5d(CUtensorMap *map, const void *base, uint64_t page_size, uint64_t H,
+                               uint64_t num_pages);
 // Row-major [outer, mid, rows, inner] bf16 tensor as a 4-D TMA map with a
 // (64 x box_rows x 1 x 1) box and 128-byte swizzle (K/V page pools).
 bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,

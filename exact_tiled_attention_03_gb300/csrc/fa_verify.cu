@@ -135,11 +135,46 @@ __device__ __forceinline__ uint32_t ld_bf16x2_or_zero(const __nv_bfloat16 *p, bo
     return valid ? *reinterpret_cast<const uint32_t *>(p) : 0u;
 }
 
-template <int D, bool kPaged>
+// 5-D tiled load, coordinates innermost first.
+__device__ __forceinline__ void tma_load_5d_hint(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                                 int32_t c4, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3), "r"(c4), "l"(policy)
+        : "memory");
+}
+
+// Where key row `key` (0-63 of a stage), 64-column half `half` and 16-byte
+// chunk `chunk` of a K or V tile sit in the stage. Layout 0 (contiguous and
+// pages of 64 keys or more, and d = 64): one 128-byte-swizzled box of 64 rows
+// per half. Layout 1 (pages of 16 or 32 keys at d = 128): one box per page,
+// its rows 256 bytes wide (both halves, so the page loads as one contiguous
+// read), the 128-byte lines swizzled in order.
+template <int kLayout>
+__device__ __forceinline__ uint32_t kv_offset(int key, int half, uint32_t chunk, int page_shift)
+{
+    if constexpr (kLayout == 0) {
+        return half * kBoxBytes + sw128_offset(static_cast<uint32_t>(key), chunk);
+    } else {
+        const uint32_t pg = static_cast<uint32_t>(key) >> page_shift;
+        const uint32_t line = ((static_cast<uint32_t>(key) & ((1u << page_shift) - 1u)) << 1) + half;
+        return (pg << (page_shift + 8)) + sw128_offset(line, chunk);
+    }
+}
+
+// kKv: 0 contiguous K/V; 1 paged, layout 0; 2 paged, layout 1 (pages of 16
+// or 32 keys at d = 128).
+template <int D, int kKv>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_verify_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const Params p)
 {
+    constexpr bool kPaged = kKv != 0;
+    constexpr int kLayout = kKv == 2 ? 1 : 0;
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -214,6 +249,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                         tma_load_3d_hint(dst + C::kTileBytes + q * kBoxBytes, &tm_v,
                                          &bars->full[s], q * 64, key, bh, pol);
                     }
+            } else if (kKv == 2) {
+                // One box per page: all rows of the page, both halves (P * 256
+                // contiguous bytes of K, and of V).
+                for (int sub = 0; sub < kStageKeys / P; ++sub) {
+                    const int pid = page_of(key / P + sub);
+                    if (lane == 0) {
+                        tma_load_5d_hint(dst + sub * P * 256, &tm_k, &bars->full[s], 0, 0, 0, h,
+                                         pid, pol);
+                        tma_load_5d_hint(dst + C::kTileBytes + sub * P * 256, &tm_v,
+                                         &bars->full[s], 0, 0, 0, h, pid, pol);
+                    }
+                }
             } else if (P >= kStageKeys) {
                 const int pid = page_of(key / P);
                 if (lane == 0)
@@ -281,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int v_key = warp * 16 + ((mi & 1) << 3) + mr;   // V: matrices (keys lo/hi) x (d lo/hi)
     const int v_half = mi >> 1;
     const uint32_t smem_a = smem_u32(smem);
+    const int page_shift = kLayout == 1 ? (p.page_size == 16 ? 4 : 5) : 0;
 
     bool ok = true;
     for (int st = 0; st < n_st && ok; ++st) {
@@ -296,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t chunk = 2 * (kk % 4) + k_half;
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(sK + (kk / 4) * kBoxBytes + sw128_offset(k_key, chunk), b0, b1, b2, b3);
+            ldsm_x4(sK + kv_offset<kLayout>(k_key, kk / 4, chunk, page_shift), b0, b1, b2, b3);
             mma_bf16_16816(sc[0], qa[kk], b0, b1);
             mma_bf16_16816(sc[1], qa[kk], b2, b3);
         }
@@ -353,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int dd = 0; dd < D / 16; ++dd) {
             const uint32_t chunk = 2 * (dd % 4) + v_half;
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(sV + (dd / 4) * kBoxBytes + sw128_offset(v_key, chunk), b0, b1, b2,
+            ldsm_x4_trans(sV + kv_offset<kLayout>(v_key, dd / 4, chunk, page_shift), b0, b1, b2,
                           b3);
             mma_bf16_16816(o[2 * dd], pa, b0, b1);
             mma_bf16_16816(o[2 * dd + 1], pa, b2, b3);
@@ -470,10 +518,15 @@ fa_status_t launch(const Problem &pr, int n_split, void *ws, size_t ws_bytes,
     using C = Cfg<D>;
     const int64_t BH = pr.B * pr.H;
     const bool paged = opt.block_table != nullptr;
+    const bool small_pages = paged && D == 128 && opt.page_size < kStageKeys;
     CUtensorMap tk, tv;
     if (!paged) {
         if (!encode_tmap_bf16_3d(&tk, pr.k, D, pr.Sk, BH, kStageKeys) ||
             !encode_tmap_bf16_3d(&tv, pr.v, D, pr.Sk, BH, kStageKeys))
+            return FA_ERR_CUDA;
+    } else if (small_pages) {
+        if (!encode_tmap_bf16_pages_5d(&tk, pr.k, opt.page_size, pr.H, opt.num_pages) ||
+            !encode_tmap_bf16_pages_5d(&tv, pr.v, opt.page_size, pr.H, opt.num_pages))
             return FA_ERR_CUDA;
     } else {
         const uint32_t box_rows =
@@ -514,7 +567,8 @@ fa_status_t launch(const Problem &pr, int n_split, void *ws, size_t ws_bytes,
     }
     if (BH > 65535)
         return FA_ERR_UNSUPPORTED;
-    auto kern = paged ? fa_verify_split_kernel<D, true> : fa_verify_split_kernel<D, false>;
+    auto kern = small_pages ? fa_verify_split_kernel<D, 2>
+                            : (paged ? fa_verify_split_kernel<D, 1> : fa_verify_split_kernel<D, 0>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return FA_ERR_CUDA;
