@@ -8,7 +8,9 @@ of the tiled prefill kernel). Prints ONE JSON line on rank 0.
   e2e       same metric through the C ABI call that takes host buffers
             (fa_forward_host) with pinned host memory: every step's H2D of
             Q, K, V and D2H of O, LSE are inside the timed region
-  roofline  achieved / measured bf16 tensor peak for the prefill kernel
+  roofline  achieved / measured bf16 tensor peak for the prefill kernel (with
+            --workload of Sq <= 16, achieved GB/s / measured HBM bandwidth for
+            the verify kernel fa_forward runs those shapes on)
   verify    the decode-shaped split-KV path (B=16, H=32, Sq=5, Sk=4096) against
             the measured HBM bandwidth (also as a draft tree and from paged caches)
   backward  dQ, dK, dV on the same workload (2.5x the forward's FLOPs)
@@ -119,9 +121,9 @@ BWD_SOURCES = ["exact_tiled_attention_03_gb300/csrc/fa_backward_sm103.cu",
                "exact_tiled_attention_03_gb300/csrc/fa_ptx.cuh"]
 
 
-def ncu_traffic(kernel: str, sources, units_per_launch: float):
-    """DRAM bytes per launch from the committed ncu summary, scaled to this
-    launch by the units processed; None if the kernel changed since."""
+def ncu_traffic(kernel: str, sources, workload: str):
+    """DRAM bytes per launch from the committed ncu summary; None if the
+    kernel changed since or the capture was of another workload."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -129,7 +131,9 @@ def ncu_traffic(kernel: str, sources, units_per_launch: float):
         d = json.load(f).get(kernel)
     if not d or d.get("source_sha") != source_hash(sources):
         return None
-    return d["dram_bytes"] * units_per_launch / d["units"]
+    if d["workload"].split()[0] != workload:
+        return None
+    return d["dram_bytes"] / d["units"]
 
 
 class ClockSampler:
@@ -347,7 +351,7 @@ def measure_backward(w, device, sptr, args, peaks):
     return {"workload": w.name, "ms_per_step": per * 1e3, "TFLOP/s": tf,
             "frac_bf16_peak": tf / peaks["bf16_tflops"], "flops_per_step": flops,
             "launches_per_step": 3, "kernels": "prep + dK/dV (4 GEMMs) + dQ (3 GEMMs)",
-            "traffic": {k: ncu_traffic(k, BWD_SOURCES, 1.0)
+            "traffic": {k: ncu_traffic(k, BWD_SOURCES, w.name)
                         for k in ("fa_bwd_dkdv_kernel<128>", "fa_bwd_dq_kernel<128>")}}
 
 
@@ -414,7 +418,7 @@ def measure_fp8(w, device, sptr, args, peaks):
             "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)",
             "frac": tf / peak, "dtype": "e4m3 in, fp32 accumulate, bf16 out",
             "launches_per_step": 1,
-            "traffic": ncu_traffic("fa_prefill_fp8_kernel", FP8_SOURCES, 1.0)}
+            "traffic": ncu_traffic("fa_prefill_fp8_kernel", FP8_SOURCES, w.name)}
 
 
 def measure_verify_variants(wv, device, sptr, args, peaks):
@@ -522,8 +526,28 @@ def run_ours(args, world, rank, local):
     flops_all = reduce_sum(float(w.exact_flops() * args.steps), world, device)
     value = flops_all / dt_max / 1e12
     per_launch_s = dt / args.steps
-    achieved = w.exact_flops() / per_launch_s / 1e12
     clocks = clk.summary(t0, t1)
+    # fa_forward runs decode-shaped problems (Sq <= FA_VERIFY_MAX_SQ) on the
+    # split-KV verify kernel, which is bound by HBM, and the rest on the prefill
+    # kernel, bound by the tensor pipe
+    if 0 < w.Sq <= _capi.FA_VERIFY_MAX_SQ:
+        gbs = w.io_bytes() / per_launch_s / 1e9
+        ns = _capi.fa_verify_auto_splits(w.B, w.H, w.Sq, w.Sk, w.d)
+        launches_per_step = 1 if ns == 1 else 2
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} HBM copy",
+                    "kernel": "fa_verify_split_kernel", "n_split": ns,
+                    "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, w.name)}
+    else:
+        achieved = w.exact_flops() / per_launch_s / 1e12
+        launches_per_step = 1
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                    "peak_source": f"{peaks['source']} bf16 burst",
+                    "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
+                    "peak_sustained": peaks["bf16_tflops_sustained"],
+                    "kernel": "fa_prefill_kernel<128>",
+                    "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, w.name)}
 
     # end to end through the C ABI call that takes host buffers (fa_forward_host):
     # pinned host inputs and outputs, every step's host-to-device and
@@ -583,7 +607,7 @@ def run_ours(args, world, rank, local):
                   "hbm_peak_GB/s": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
                   "bytes_per_step": wv.io_bytes(), "n_split": n_split,
                   "launches_per_step": 1 if n_split == 1 else 2,
-                  "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, 1.0)}
+                  "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, wv.name)}
         del qv, kv_, vv, ov, lv, ws
 
     # the backward pass on the same workload (dQ, dK, dV by recomputation from
@@ -634,20 +658,14 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": config_block(w, world),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                         "peak_source": f"{peaks['source']} bf16 burst",
-                         "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "peak_sustained": peaks["bf16_tflops_sustained"],
-                         "kernel": "fa_prefill_kernel<128>",
-                         "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, 1.0)},
+            "roofline": roofline,
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
             "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "backward": backward,
             "fp8": fp8, "forward_other": forward_other, "exp_pipe": exp_pipe, "mma_rate": mma_rate,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": args.steps,  # one prefill kernel per timed step
+            "gpu_launches": args.steps * launches_per_step,
             "gpu": torch.cuda.get_device_name(device),
         }
         print(json.dumps(line), flush=True)
