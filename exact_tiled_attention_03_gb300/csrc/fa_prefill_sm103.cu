@@ -64,6 +64,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (16 KB)
 // Lazy rescale threshold, in log2 units of the exponent (factor 256).
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleFactor = 256.0f;  // 2^kRescaleLog2
 
 template <int D>
 struct Cfg {
@@ -414,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float2 acc[4];
                 // One pass over S_t in chunks of kChunk columns: load, mask, and
                 // (when `with_exp`) p = 2^(s*sl2 + neg), accumulated into acc and
-                // packed into pk. Returns the max of the raw scores it saw.
-                auto pass = [&](bool with_exp, float neg) {
+                // packed into pk. Returns the max of the raw scores (when
+                // `with_max`; -inf otherwise).
+                auto pass = [&](bool with_exp, bool with_max, float neg) {
                     const float2 negx2 = make_float2(neg, neg);
                     float mx = -INFINITY;
 #pragma unroll
@@ -433,18 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (key0 + c0 + c >= lim)
                                     sv[c] = -INFINITY;
                         }
-                        float part[kChunk / 16];
+                        if (with_max) {
+                            float part[kChunk / 16];
 #pragma unroll
-                        for (int k = 0; k < kChunk / 16; ++k) {
-                            float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
+                            for (int k = 0; k < kChunk / 16; ++k) {
+                                float x = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
 #pragma unroll
-                            for (int e = 3; e < 15; e += 2)
-                                x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
-                            part[k] = fmaxf(x, sv[16 * k + 15]);
+                                for (int e = 3; e < 15; e += 2)
+                                    x = fmax3(x, sv[16 * k + e], sv[16 * k + e + 1]);
+                                part[k] = fmaxf(x, sv[16 * k + 15]);
+                            }
+#pragma unroll
+                            for (int k = 0; k < kChunk / 16; ++k)
+                                mx = fmaxf(mx, part[k]);
                         }
-#pragma unroll
-                        for (int k = 0; k < kChunk / 16; ++k)
-                            mx = fmaxf(mx, part[k]);
                         if (with_exp) {
 #pragma unroll
                             for (int c = 0; c < kChunk / 2; ++c) {
@@ -464,43 +468,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     return mx;
                 };
-                // Speculative pass: when every lane already has a reference max,
-                // the exponentials are computed against it while the tile's max
-                // is found.
-                const bool spec = __all_sync(0xffffffffu, m != -INFINITY);
-                const float mx = pass(spec, spec ? -m * sl2 : 0.0f);
-                // The reference moves only when the tile's max exceeds it by more
-                // than 2^kRescaleLog2 (or on the first visible key); O and l always
-                // share it, so the result stays exact and P stays <= 2^kRescaleLog2.
-                // NaN (both -inf) compares false: nothing visible yet, keep m.
-                const float m_new = fmaxf(m, mx);
-                const bool move = (m_new - m) * sl2 > kRescaleLog2;
-                const float m_use = move ? m_new : m;
-                const float corr = move ? ex2_approx((m - m_use) * sl2) : 1.0f;  // 0 when m = -inf
-                if (!spec || __any_sync(0xffffffffu, move)) {
-                    // Second pass with the moved reference (lanes that did not move
-                    // recompute the same values). S_t is still intact: P has not
-                    // been written yet.
-                    pass(true, (m_use == -INFINITY) ? 0.0f : -m_use * sl2);
-                    // O_t *= corr (warp-uniform; lanes that did not move multiply
-                    // by 1). PV_t(j-1) has completed: S_t(j), committed after it,
-                    // is done.
-                    if (j > 0 && __any_sync(0xffffffffu, move)) {
-                        const float2 cx2 = make_float2(corr, corr);
+                // The reference max m moves only when the tile's max exceeds it by
+                // more than 2^kRescaleLog2 (or on the first visible key); O and l
+                // always share it, so the result stays exact and P stays <=
+                // 2^kRescaleLog2. NaN (both -inf) compares false: nothing visible
+                // yet, keep m. Until P is written, S_t is intact and may be read
+                // again.
+                float m_use = m, corr = 1.0f;
+                bool any_move = false;  // some lane of the warp moved its reference
+                auto decide = [&](float mx) {
+                    const float m_new = fmaxf(m, mx);
+                    const bool move = (m_new - m) * sl2 > kRescaleLog2;
+                    m_use = move ? m_new : m;
+                    corr = move ? ex2_approx((m - m_use) * sl2) : 1.0f;  // 0 when m = -inf
+                    any_move = __any_sync(0xffffffffu, move);
+                };
+                // O_t *= corr after a move (warp-uniform; lanes that did not move
+                // multiply by 1). PV_t(j-1) has completed: S_t(j), committed after
+                // it, is done.
+                auto rescale_o = [&]() {
+                    if (j == 0 || !any_move)
+                        return;
+                    const float2 cx2 = make_float2(corr, corr);
 #pragma unroll
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t o[32];
-                            tmem_ld32_wait(tO + c0, o);
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32_wait(tO + c0, o);
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
-                                                                   __uint_as_float(o[2 * c + 1])),
-                                                       cx2);
-                                o[2 * c] = __float_as_uint(v.x);
-                                o[2 * c + 1] = __float_as_uint(v.y);
-                            }
-                            tmem_st32(tO + c0, o);
+                        for (int c = 0; c < 16; ++c) {
+                            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * c]),
+                                                               __uint_as_float(o[2 * c + 1])),
+                                                   cx2);
+                            o[2 * c] = __float_as_uint(v.x);
+                            o[2 * c + 1] = __float_as_uint(v.y);
                         }
+                        tmem_st32(tO + c0, o);
+                    }
+                };
+                if constexpr (D == 128) {
+                    // Speculative pass without the max: when every lane has a
+                    // reference, p is computed against it. Every p is >= 0, so a row
+                    // sum of at most 2^kRescaleLog2 shows that no p exceeds
+                    // 2^kRescaleLog2 and m stays; a larger sum sends the warp to the
+                    // max pass and then to the exponentials against m_use. The
+                    // passes run one per iteration of this loop, so the code holds
+                    // one copy of the pass (three copies spilled at 168 registers).
+                    // Stages: 0 speculative exponentials, 1 max, 2 exponentials.
+                    int stage = __all_sync(0xffffffffu, m != -INFINITY) ? 0 : 1;
+#pragma unroll 1
+                    while (true) {
+                        const bool with_exp = stage != 1;
+                        const float neg =
+                            stage == 0 ? -m * sl2 : ((m_use == -INFINITY) ? 0.0f : -m_use * sl2);
+                        const float mx = pass(with_exp, !with_exp, neg);
+                        if (stage == 0) {
+                            const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+                            if (!__any_sync(0xffffffffu, a.x + a.y > kRescaleFactor))
+                                break;
+                            stage = 1;
+                        } else if (stage == 1) {
+                            decide(mx);
+                            stage = 2;
+                        } else {
+                            rescale_o();
+                            break;
+                        }
+                    }
+                } else {
+                    // d = 64: the speculative pass finds the tile's max while it
+                    // computes p against m (the form above measured 1.07x slower
+                    // at this head dim); a second pass follows when m moves.
+                    const bool spec = __all_sync(0xffffffffu, m != -INFINITY);
+                    decide(pass(spec, true, spec ? -m * sl2 : 0.0f));
+                    if (!spec || any_move) {
+                        pass(true, true, (m_use == -INFINITY) ? 0.0f : -m_use * sl2);
+                        rescale_o();
                     }
                 }
                 // P (bf16 pairs) over S_t's first 64 columns, then publish.
