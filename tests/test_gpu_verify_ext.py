@@ -113,21 +113,64 @@ def test_paged_kv_matches_per_sequence_oracle(page_size, mode, n_split):
         compare(o[b:b + 1], lse[b:b + 1], ro, rl)
 
 
-def test_paged_kv_with_contiguous_pages_equals_contiguous_path():
-    """Pages laid out in order reproduce the contiguous verify kernel exactly."""
-    w = custom(2, 4, 5, 1024, 128, True, seed=29)
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("n_split", [0, 3])
+def test_paged_kv_head_dim_64(page_size, n_split):
+    """d = 64 pages (128-byte rows: one box per page at every page size)."""
+    B, H, Sq, d, Smax = 3, 2, 5, 64, 520
+    lens = [520, 77, 200]
+    w = custom(B, H, Sq, Smax, d, True, seed=31 * page_size + n_split)
     q, k, v = make_qkv(w)
-    P = 64
-    kp = k.reshape(2, 4, 1024 // P, P, 128).permute(0, 2, 1, 3, 4).reshape(-1, 4, P, 128).contiguous()
-    vp = v.reshape(2, 4, 1024 // P, P, 128).permute(0, 2, 1, 3, 4).reshape(-1, 4, P, 128).contiguous()
-    table = torch.arange(2 * 16, dtype=torch.int32).reshape(2, 16)
-    lens = torch.tensor([1024, 1024], dtype=torch.int32)
-    o_p, l_p = run_paged(q, kp, vp, table, lens, P, 1024, True, None, w.scale, 4)
-    o = torch.empty((2, 4, 5, 128), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((2, 4, 5), device="cuda")
-    need = _capi.fa_verify_workspace_size(2, 4, 5, 1024, 128, 4)
+    kp, vp, table, lens_t = make_paged_kv(k, v, lens, page_size, seed=page_size + 1)
+    o, lse = run_paged(q, kp, vp, table, lens_t, page_size, Smax, True, None, w.scale, n_split)
+    for b in range(B):
+        Sk = lens[b]
+        ro, rl = oracle.attention(q[b:b + 1], k[b:b + 1, :, :Sk], v[b:b + 1, :, :Sk], True, w.scale)
+        compare(o[b:b + 1], lse[b:b + 1], ro, rl)
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+def test_paged_kv_entries_outside_the_pool_read_as_zeros(page_size):
+    """A block-table entry outside [0, num_pages) reads as zero K and V rows."""
+    B, H, Sq, d, Smax = 2, 3, 5, 128, 700
+    lens = [700, 333]
+    w = custom(B, H, Sq, Smax, d, True, seed=41 + page_size)
+    q, k, v = make_qkv(w)
+    kp, vp, table, lens_t = make_paged_kv(k, v, lens, page_size, seed=page_size + 2)
+    num_pages = kp.shape[0]
+    table[0, 3] = num_pages + 3
+    table[1, 1] = -1
+    k_log, v_log = k.clone(), v.clone()
+    for b, lp in ((0, 3), (1, 1)):
+        k_log[b, :, lp * page_size:(lp + 1) * page_size] = 0
+        v_log[b, :, lp * page_size:(lp + 1) * page_size] = 0
+    o, lse = run_paged(q, kp, vp, table, lens_t, page_size, Smax, True, None, w.scale, 0)
+    for b in range(B):
+        Sk = lens[b]
+        ro, rl = oracle.attention(q[b:b + 1], k_log[b:b + 1, :, :Sk], v_log[b:b + 1, :, :Sk], True,
+                                  w.scale)
+        compare(o[b:b + 1], lse[b:b + 1], ro, rl)
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("d", [64, 128])
+def test_paged_kv_with_contiguous_pages_equals_contiguous_path(page_size, d):
+    """Pages laid out in order reproduce the contiguous verify kernel exactly,
+    whatever box layout the page size selects."""
+    B, H, S = 2, 4, 1024
+    w = custom(B, H, 5, S, d, True, seed=29)
+    q, k, v = make_qkv(w)
+    P = page_size
+    kp = k.reshape(B, H, S // P, P, d).permute(0, 2, 1, 3, 4).reshape(-1, H, P, d).contiguous()
+    vp = v.reshape(B, H, S // P, P, d).permute(0, 2, 1, 3, 4).reshape(-1, H, P, d).contiguous()
+    table = torch.arange(B * (S // P), dtype=torch.int32).reshape(B, S // P)
+    lens = torch.tensor([S] * B, dtype=torch.int32)
+    o_p, l_p = run_paged(q, kp, vp, table, lens, P, S, True, None, w.scale, 4)
+    o = torch.empty((B, H, 5, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, 5), device="cuda")
+    need = _capi.fa_verify_workspace_size(B, H, 5, S, d, 4)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    _capi.check(_capi.fa_verify_forward(q.cuda(), k.cuda(), v.cuda(), o, lse, 2, 4, 5, 1024, 128, 1,
+    _capi.check(_capi.fa_verify_forward(q.cuda(), k.cuda(), v.cuda(), o, lse, B, H, 5, S, d, 1,
                                         w.scale, 4, ws, need), "fa_verify_forward")
     torch.cuda.synchronize()
     assert torch.equal(o.float().cpu(), o_p) and torch.equal(lse.cpu(), l_p)
