@@ -134,6 +134,30 @@ def make_qkv(w: Workload, device="cpu"):
     return q, k, v
 
 
+def make_qkv_device(w: Workload, device="cuda"):
+    """Q, K, V for workload ``w`` drawn on ``device`` by a seeded device
+    generator, for shapes too large to draw on the host (tensors past 2^31
+    elements). Same recipe as ``make_qkv`` (iid N(0, 1) in fp32, Q times
+    q_factor, cast to bf16), drawn in slices of the batch dimension of about
+    2^27 elements; the values differ from ``make_qkv``'s for the same seed."""
+    g = torch.Generator(device=device).manual_seed(w.seed)
+    out = []
+    for shape, factor in ((w.q_shape, w.q_factor), (w.kv_shape, 1.0), (w.kv_shape, 1.0)):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        per_b = shape[1] * shape[2] * shape[3]
+        step = max(1, (1 << 27) // per_b)
+        for b0 in range(0, shape[0], step):
+            b1 = min(shape[0], b0 + step)
+            x = torch.randn((b1 - b0,) + tuple(shape[1:]), generator=g, dtype=torch.float32,
+                            device=device)
+            if factor != 1.0:
+                x.mul_(factor)
+            t[b0:b1].copy_(x)
+            del x
+        out.append(t)
+    return tuple(out)
+
+
 def make_qkv_fp8(w: Workload, device="cpu"):
     """E4M3 inputs for workload ``w``: the same N(0, 1) draws as ``make_qkv``
     (seed, order, q_factor), each tensor divided by a power-of-two descale
