@@ -215,21 +215,32 @@ def oracle_rows_flops(w, rows):
 
 def time_oracle_sample(w, q, k, v, budget_s: float, seed: int = 7, threads: int = 0):
     """Time the oracle (as it stands) on a seeded sample of rows sized to ~budget_s
-    (threads = 0: the OpenMP default)."""
+    (threads = 0: the OpenMP default). The sample is sized from a probe large
+    enough to occupy every thread (a small probe is dominated by per-call costs
+    and would size the sample short), and topped up once if it still ran under
+    60 % of the budget."""
     import oracle
 
-    probe = sample_rows(w, n_total=16, seed=seed)
-    t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.causal, w.scale, rows=probe, threads=threads)
-    dt = max(time.perf_counter() - t0, 1e-6)
-    per_flop = dt / oracle_rows_flops(w, probe)
-    avg_row = w.exact_flops() / (w.B * w.H * w.Sq)
-    n = int(max(16, min(w.B * w.H * w.Sq, budget_s / (per_flop * avg_row))))
-    rows = sample_rows(w, n_total=n, seed=seed + 1)
-    t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads)
-    dt = time.perf_counter() - t0
-    return rows, dt, oracle_rows_flops(w, rows)
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads)
+        return time.perf_counter() - t0
+
+    total = w.B * w.H * w.Sq
+    probe = sample_rows(w, n_total=min(64 if threads == 1 else 512, total), seed=seed)
+    per_flop = max(run(probe), 1e-6) / oracle_rows_flops(w, probe)
+    avg_row = w.exact_flops() / total
+    rows, dt, fl = [], 0.0, 0.0
+    for attempt in range(2):
+        n = int(max(16, min(total, (budget_s - dt) / (per_flop * avg_row))))
+        r = sample_rows(w, n_total=n, seed=seed + 1 + attempt)
+        dt += run(r)
+        fl += oracle_rows_flops(w, r)
+        rows += r
+        if dt >= 0.6 * budget_s or n >= total:
+            break
+        per_flop = dt / fl
+    return rows, dt, fl
 
 
 def measure_exp_pipe(w, device, sptr):
@@ -681,7 +692,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
