@@ -63,6 +63,23 @@ def test_inputs_are_seeded_and_bf16():
     assert qs.float().abs().max() > 2 * a[0].float().abs().max()
 
 
+def test_device_inputs_are_seeded_and_bf16():
+    """make_qkv_device (the generator of the largest GPU cases), run here with the
+    CPU generator: seeded, bf16, contiguous, with the recipe's N(0, 1) statistics
+    and q_factor."""
+    from exact_tiled_attention_03_gb300 import inputs
+
+    w = custom(3, 2, 64, 80, 16, True, seed=9)
+    a = inputs.make_qkv_device(w, "cpu")
+    b = inputs.make_qkv_device(w, "cpu")
+    for x, y in zip(a, b):
+        assert x.dtype == torch.bfloat16 and x.is_contiguous() and torch.equal(x, y)
+    assert a[0].shape == (3, 2, 64, 16) and a[1].shape == (3, 2, 80, 16)
+    assert abs(float(a[1].float().std()) - 1.0) < 0.05 and abs(float(a[2].float().mean())) < 0.05
+    q4 = inputs.make_qkv_device(custom(3, 2, 64, 80, 16, True, seed=9, q_factor=4.0), "cpu")[0]
+    assert abs(float(q4.float().std()) / float(a[0].float().std()) - 4.0) < 0.1
+
+
 def test_scale_is_fp32_of_inverse_sqrt_d():
     for d in (64, 128):
         w = custom(1, 1, 1, 1, d, False)
