@@ -29,10 +29,12 @@
 //   * warps 0-3 and 4-7 are one softmax warpgroup per query tile; thread r
 //     owns row r (TMEM lane r). It streams its S row out of TMEM in 64-column
 //     chunks, masks, and computes exp2 of the log2(e)-scaled logits against
-//     its current reference max while it finds the tile's max; only if that
-//     max exceeds the reference by more than 2^8 (or on the row's first
-//     tile) does it recompute the row against the new max and rescale its O
-//     row in TMEM. It then writes P (bf16) over its S row in TMEM. At the end
+//     its current reference max (at d = 64 while it finds the tile's max; at
+//     d = 128 without it, the row sum of those exponentials showing whether
+//     any exceeds 2^8); only if the tile's max exceeds the reference by more
+//     than 2^8 (or on the row's first tile) does it recompute the row against
+//     the new max and rescale its O row in TMEM. It then writes P (bf16) over
+//     its S row in TMEM. At the end
 //     of an item it divides by l and writes its bf16 O row into the tile's
 //     own staging box in shared memory, 64 columns at a time, each box sent
 //     by one TMA store; then it writes its LSE. Q's buffers are reloaded for
