@@ -488,6 +488,31 @@ def measure_verify_variants(wv, device, sptr, args, peaks):
 
 
 
+def main_roofline(w, per_launch_s: float, peaks, n_split: int):
+    """The roofline object of the main line and the launches per step.
+    fa_forward runs decode-shaped problems (Sq <= FA_VERIFY_MAX_SQ) on the
+    split-KV verify kernel, which is bound by HBM (n_split > 1 adds the combine
+    launch), and the rest on the prefill kernel, bound by the tensor pipe."""
+    from exact_tiled_attention_03_gb300._capi import FA_VERIFY_MAX_SQ
+
+    if 0 < w.Sq <= FA_VERIFY_MAX_SQ:
+        gbs = w.io_bytes() / per_launch_s / 1e9
+        return ({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} HBM copy",
+                 "kernel": "fa_verify_split_kernel", "n_split": n_split,
+                 "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, w.name)},
+                1 if n_split == 1 else 2)
+    achieved = w.exact_flops() / per_launch_s / 1e12
+    return ({"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+             "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+             "peak_source": f"{peaks['source']} bf16 burst",
+             "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
+             "peak_sustained": peaks["bf16_tflops_sustained"],
+             "kernel": "fa_prefill_kernel<128>",
+             "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, w.name)},
+            1)
+
+
 def config_block(w, world):
     return {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
             "causal": w.causal, "scale": w.scale, "parallelism": f"replicas x{world}",
@@ -538,27 +563,9 @@ def run_ours(args, world, rank, local):
     value = flops_all / dt_max / 1e12
     per_launch_s = dt / args.steps
     clocks = clk.summary(t0, t1)
-    # fa_forward runs decode-shaped problems (Sq <= FA_VERIFY_MAX_SQ) on the
-    # split-KV verify kernel, which is bound by HBM, and the rest on the prefill
-    # kernel, bound by the tensor pipe
-    if 0 < w.Sq <= _capi.FA_VERIFY_MAX_SQ:
-        gbs = w.io_bytes() / per_launch_s / 1e9
-        ns = _capi.fa_verify_auto_splits(w.B, w.H, w.Sq, w.Sk, w.d)
-        launches_per_step = 1 if ns == 1 else 2
-        roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} HBM copy",
-                    "kernel": "fa_verify_split_kernel", "n_split": ns,
-                    "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, w.name)}
-    else:
-        achieved = w.exact_flops() / per_launch_s / 1e12
-        launches_per_step = 1
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "peak_source": f"{peaks['source']} bf16 burst",
-                    "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "peak_sustained": peaks["bf16_tflops_sustained"],
-                    "kernel": "fa_prefill_kernel<128>",
-                    "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, w.name)}
+    ns = (_capi.fa_verify_auto_splits(w.B, w.H, w.Sq, w.Sk, w.d)
+          if 0 < w.Sq <= _capi.FA_VERIFY_MAX_SQ else 0)
+    roofline, launches_per_step = main_roofline(w, per_launch_s, peaks, ns)
 
     # end to end through the C ABI call that takes host buffers (fa_forward_host):
     # pinned host inputs and outputs, every step's host-to-device and

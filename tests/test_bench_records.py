@@ -48,3 +48,24 @@ def test_a_record_is_used_only_for_its_own_workload():
 def test_unknown_kernel_has_no_record():
     assert bench.ncu_traffic("no_such_kernel", bench.PREFILL_SOURCES,
                              "prefill_b4h32s8192d128_causal") is None
+
+
+def test_main_roofline_follows_the_kernel_fa_forward_dispatches_to():
+    """Decode shapes (Sq <= 16) run on the split-KV verify kernel and are read
+    against HBM; the rest run on the prefill kernel and are read against the
+    bf16 tensor peak."""
+    from exact_tiled_attention_03_gb300.inputs import WORKLOADS
+
+    peaks = {"bf16_tflops": 1000.0, "bf16_tflops_sustained": 900.0, "hbm_gbs": 5000.0,
+             "source": "test"}
+    wv = WORKLOADS["verify_b16h32q5k4096d128"]
+    r, launches = bench.main_roofline(wv, 200e-6, peaks, 4)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and launches == 2
+    assert abs(r["achieved"] - wv.io_bytes() / 200e-6 / 1e9) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 5000.0) < 1e-12
+    assert bench.main_roofline(wv, 200e-6, peaks, 1)[1] == 1
+    wp = WORKLOADS["prefill_b4h32s2048d128_causal"]
+    r, launches = bench.main_roofline(wp, 1e-3, peaks, 0)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and launches == 1
+    assert abs(r["achieved"] - wp.exact_flops() / 1e-3 / 1e12) < 1e-9
+    assert r["traffic"] is None  # the committed capture is of another workload
