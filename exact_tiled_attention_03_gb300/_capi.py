@@ -51,6 +51,7 @@ SIGNATURES = {
     "fa_selftest_umma_ts": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_umma_f8": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_wait_timeout": (_I32, [_U64, _P]),
+    "fa_testing_stall_next_launch": (_I32, [_I32, _I32, _U64]),
     "fa_selftest_mufu": (_I32, [_P, _I32, _I32, _P]),
     "fa_selftest_mma_rate": (_I32, [_P, _I32, _I32, _I32, _P]),
 }
@@ -236,6 +237,14 @@ def fa_selftest_mma_rate(cycles, mode, blocks, iters, stream=None) -> int:
 
 def fa_selftest_wait_timeout(timeout_ns, stream=None) -> int:
     return load().fa_selftest_wait_timeout(int(timeout_ns), _stream(stream))
+
+
+def fa_testing_stall_next_launch(kernel, skip_index, wait_limit_ns) -> int:
+    return load().fa_testing_stall_next_launch(int(kernel), int(skip_index), int(wait_limit_ns))
+
+
+STALL_PREFILL = 1
+STALL_VERIFY = 2
 
 
 def check(status: int, what: str = "fa call"):

@@ -1,7 +1,7 @@
 // fa_abi.cu — the C ABI declared in include/fa.h and include/fa_testing.h:
 // argument validation, shape dispatch (prefill vs split-KV), TMA descriptor
-// encoding, the device status word, and the stream-ordered workspace of
-// fa_forward. No compute happens here.
+// encoding, the device status word, and the library's stream-ordered
+// workspace pool. No compute happens here.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -19,31 +19,57 @@ __device__ unsigned int g_fa_status_word;
 __device__ unsigned long long g_fa_work_slots[2 * fa::kWorkSlots];
 
 namespace fa {
+
+void *current_context()
+{
+    using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS)
+        return nullptr;
+    return ctx;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     bool ready = false;
+    void *ctx = nullptr;  // the CUDA context the addresses below belong to
     int num_sms = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned int *status = nullptr;
     unsigned long long *work = nullptr;
+    cudaMemPool_t pool = nullptr;  // library pool for small workspaces (created on first use)
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
-// Per-device facts and the device address of the status word, looked up once
-// per device with that device current.
+// Per-device facts and the device addresses of the status word and the work
+// counters, looked up with the device current and kept while the calling
+// thread's CUDA context stays the one they were looked up in (a device reset
+// or a caller-made driver context triggers a fresh lookup).
 const DeviceInfo *device_info()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return nullptr;
+    void *ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceInfo &di = g_dev[dev];
-    if (!di.ready) {
+    if (!di.ready || ctx != di.ctx) {
+        di.ready = false;
         if (cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
@@ -55,9 +81,44 @@ const DeviceInfo *device_info()
         if (cudaGetSymbolAddress(&addr, g_fa_work_slots) != cudaSuccess)
             return nullptr;
         di.work = static_cast<unsigned long long *>(addr);
+        di.ctx = current_context();  // the runtime has bound its context by now
+        di.pool = nullptr;
         di.ready = true;
     }
     return &di;
+}
+
+// The library's stream-ordered memory pool on the current device, for the
+// small workspaces fa_forward (split-KV partials) and fa_backward (per-row
+// vectors) take when the caller passes none. Freed blocks stay in the pool
+// (release threshold: never), so the next call's allocation is a
+// suballocation, not a request to the driver at every synchronisation as
+// with the device's default pool. nullptr on failure.
+cudaMemPool_t library_pool(const DeviceInfo *cdi)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (&di != cdi || !di.ready)
+        return nullptr;
+    if (!di.pool) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess)
+            return nullptr;
+        uint64_t keep = UINT64_MAX;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return nullptr;
+        }
+        di.pool = pool;
+    }
+    return di.pool;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -73,8 +134,6 @@ fa_status_t validate(const void *q, const void *k, const void *v, const void *o,
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale))
         return FA_ERR_INVALID_ARG;
-    if (!(scale > 0.0f))
-        return FA_ERR_UNSUPPORTED;
     if (any_d ? (d > 128) : (d != 64 && d != 128))
         return FA_ERR_UNSUPPORTED;
     const int64_t lim31 = (int64_t(1) << 31) - 1;
@@ -221,6 +280,41 @@ int verify_splits_or_auto(int n_split, int64_t BH, int64_t Sk, const DeviceInfo 
 
 }  // namespace
 
+namespace {
+struct StallRequest {
+    int kernel = 0;  // 0: none pending
+    int skip = -1;
+    uint64_t wait_ns = 0;
+};
+std::mutex g_stall_mu;
+StallRequest g_stall;
+}  // namespace
+
+void take_stall(int kernel, int *skip_index, uint64_t *wait_ns)
+{
+    std::lock_guard<std::mutex> lock(g_stall_mu);
+    if (g_stall.kernel != kernel)
+        return;
+    *skip_index = g_stall.skip;
+    *wait_ns = g_stall.wait_ns;
+    g_stall = StallRequest();
+}
+
+fa_status_t verify_check_args(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                              int64_t d, float scale, int n_split)
+{
+    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    if (st != FA_OK)
+        return st;
+    if (Sq > FA_VERIFY_MAX_SQ || B * H > 65535)
+        return FA_ERR_UNSUPPORTED;
+    const int64_t max_split = (Sk + kVerifyStageKeys - 1) / kVerifyStageKeys;
+    if (n_split < 0 || n_split > max_split || n_split > 65535)
+        return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
 bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                          uint64_t depth, uint32_t box_rows)
 {
@@ -292,7 +386,7 @@ const char *fa_status_string(fa_status_t s)
     switch (s) {
     case FA_OK: return "ok";
     case FA_ERR_INVALID_ARG: return "invalid argument";
-    case FA_ERR_UNSUPPORTED: return "unsupported shape, alignment, scale or device";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape, alignment or device";
     case FA_ERR_CUDA: return "CUDA runtime or launch error";
     case FA_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
     case FA_ERR_WORKSPACE: return "workspace missing or too small";
@@ -365,14 +459,9 @@ fa_status_t fa_verify_forward(const void *q, const void *k, const void *v, void 
                               int causal, float scale, int n_split, void *workspace,
                               size_t ws_bytes, void *stream)
 {
-    fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Sk, d, scale, false);
+    fa_status_t st = verify_check_args(q, k, v, o, lse, B, H, Sq, Sk, d, scale, n_split);
     if (st != FA_OK)
         return st;
-    if (Sq > FA_VERIFY_MAX_SQ || B * H > 65535)
-        return FA_ERR_UNSUPPORTED;
-    const int64_t max_split = (Sk + kVerifyStageKeys - 1) / kVerifyStageKeys;
-    if (n_split < 0 || n_split > max_split || n_split > 65535)
-        return FA_ERR_INVALID_ARG;
     const DeviceInfo *di = nullptr;
     if ((st = device_ok(&di)) != FA_OK)
         return st;
@@ -499,7 +588,8 @@ fa_status_t fa_backward(const void *q, const void *k, const void *v, const void 
         if (ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return FA_ERR_WORKSPACE;
     } else {
-        if (cudaMallocAsync(&workspace, need, s) != cudaSuccess)
+        cudaMemPool_t pool = library_pool(di);
+        if (!pool || cudaMallocFromPoolAsync(&workspace, need, pool, s) != cudaSuccess)
             return FA_ERR_CUDA;
         owned = true;
     }
@@ -554,8 +644,11 @@ fa_status_t fa_forward(const void *q, const void *k, const void *v, void *o, flo
     const size_t need = verify_workspace_bytes(B * H, Sq, d, ns);
     void *ws = nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess)
-        return FA_ERR_CUDA;
+    if (need > 0) {
+        cudaMemPool_t pool = library_pool(di);
+        if (!pool || cudaMallocFromPoolAsync(&ws, need, pool, s) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
     st = launch_verify(make_problem(q, k, v, o, lse, B, H, Sq, Sk, d, causal, scale, stream,
                                     di->status),
                        ns, ws, need);
@@ -778,6 +871,18 @@ fa_status_t fa_selftest_mma_rate(long long *cycles, int mode, int blocks, int it
         return st;
     return launch_selftest_mma_rate(cycles, mode, blocks, iters, static_cast<cudaStream_t>(stream),
                                     di->status);
+}
+
+fa_status_t fa_testing_stall_next_launch(int kernel, int skip_index, uint64_t wait_limit_ns)
+{
+    if ((kernel != kStallPrefill && kernel != kStallVerify) || skip_index < 0 ||
+        wait_limit_ns < 1000000ull || wait_limit_ns > 10000000000ull)
+        return FA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_stall_mu);
+    g_stall.kernel = kernel;
+    g_stall.skip = skip_index;
+    g_stall.wait_ns = wait_limit_ns;
+    return FA_OK;
 }
 
 fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream)

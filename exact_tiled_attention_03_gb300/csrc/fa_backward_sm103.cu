@@ -71,7 +71,11 @@ constexpr int kChunk = 32;               // TMEM columns a math thread handles a
 struct Params {
     int Sq, Sk, Sq_pad, BH, n_qtiles, n_ktiles;
     int causal;
-    float scale, scale_log2;
+    float scale;       // the caller's scale (signed): dK, dQ = scale * ...
+    float scale_log2;  // |scale| * log2(e), the factor of the P rebuild
+    // kIdescNegateA for a negative scale, else 0: the score MMAs then form
+    // -Q K^T (or -K Q^T), so P = 2^(scores * scale_log2 - lse2) as for scale > 0.
+    uint32_t idesc_s_neg;
     const float *lse2;  // -lse2: [BH, Sq_pad], -inf padding
     const float *Dvec;  // -D: [BH, Sq_pad], -0 padding
     unsigned int *status;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
                     umma_bf16_ss(tmem + (dp ? C::kColDP : C::kColS), a0 + koff, b0 + koff,
-                                 idesc_s, kk > 0);
+                                 dp ? idesc_s : idesc_s | p.idesc_s_neg, kk > 0);
                 }
                 umma_commit(dp ? &bars->dp_full : &bars->s_full);
             };
@@ -739,7 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + col, a0 + koff, b0 + koff, idesc_s, kk > 0);
+                    umma_bf16_ss(tmem + col, a0 + koff, b0 + koff,
+                                 dp ? idesc_s : idesc_s | p.idesc_s_neg, kk > 0);
                 }
                 if (dp) {
                     umma_commit(&bars->dp_full);
@@ -940,7 +945,8 @@ fa_status_t launch(const BackwardProblem &bp)
     p.n_ktiles = static_cast<int>((pr.Sk + kBlock - 1) / kBlock);
     p.causal = pr.causal ? 1 : 0;
     p.scale = pr.scale;
-    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.scale_log2 = fabsf(pr.scale) * 1.4426950408889634f;
+    p.idesc_s_neg = std::signbit(pr.scale) ? kIdescNegateA : 0u;
     p.lse2 = lse2;
     p.Dvec = Dvec;
     p.status = pr.status;

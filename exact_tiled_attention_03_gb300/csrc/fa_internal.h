@@ -93,6 +93,25 @@ fa_status_t launch_selftest_mufu(float *out, int blocks, int iters, cudaStream_t
 fa_status_t launch_selftest_mma_rate(long long *cycles, int mode, int blocks, int iters,
                                      cudaStream_t stream, unsigned int *status);
 
+// The calling thread's current CUDA (driver) context, or nullptr if none is
+// bound; device addresses looked up with cudaGetSymbolAddress are valid in
+// this context only.
+void *current_context();
+
+// The argument checks of fa_verify_forward (shape, pointers, scale, Sq and
+// B*H limits, split count range), in its order; touches no device.
+fa_status_t verify_check_args(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                              int64_t d, float scale, int n_split);
+
+// Test-only stall injection (fa_testing_stall_next_launch): the next launch
+// of the named kernel takes the pending request, if any (one-shot), as the
+// index of the load its first CTA's producer skips and the limit of its
+// bounded waits; without a request both outputs are left unchanged.
+constexpr int kStallPrefill = 1;
+constexpr int kStallVerify = 2;
+void take_stall(int kernel, int *skip_index, uint64_t *wait_ns);
+
 // Split-KV geometry shared by the ABI (workspace sizing) and the launcher.
 constexpr int kVerifyStageKeys = 64;
 int verify_auto_splits(int64_t BH, int64_t Sk, int num_sms);

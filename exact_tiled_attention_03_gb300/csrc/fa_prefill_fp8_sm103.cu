@@ -81,7 +81,13 @@ __device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * static_c
 
 struct Params {
     sched::Schedule sc;  // items and their order (fa_schedule.cuh)
-    float sl2;           // scale * q_descale * k_descale * log2(e)
+    float sl2;           // |scale| * q_descale * k_descale * log2(e)
+    // kIdescNegateA for a negative scale, else 0: the S MMAs then form
+    // -Q K^T, so the softmax sees the non-negative factor sl2.
+    uint32_t idesc_qk_neg;
+    // Scale 0: every score is 0 whatever Q holds, so Q tiles are read from
+    // head index BH, outside the tensor (TMA fills zeros), and sl2 = 1.
+    int zero_q;
     float v_descale;
     float *lse;
     unsigned int *status;
@@ -219,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&bars->q_full[t], kTileBytes);
-                    tma_load_3d_hint(sQ + t * kTileBytes, &tm_q, &bars->q_full[t], 0, I.q0[t], I.bh,
-                                     pol_stream);
+                    tma_load_3d_hint(sQ + t * kTileBytes, &tm_q, &bars->q_full[t], 0, I.q0[t],
+                                     p.zero_q ? p.sc.BH : I.bh, pol_stream);
                     ++q_loads[t];
                 }
                 for (int j = 1; j < I.n_kv_max && ok; ++j)
@@ -239,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_1(0), then per j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), as in the
         // bf16 kernel.
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_e4m3_f32(kBlockM, kBlockN, false, false);
+            const uint32_t idesc_qk = idesc_e4m3_f32(kBlockM, kBlockN, false, false) | p.idesc_qk_neg;
             constexpr uint32_t idesc_pv = idesc_e4m3_f32(kBlockM, kD, false, true);
             const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
             // Q and K K-major (a k-step of 32 bytes within the swizzled row);
@@ -582,10 +588,15 @@ fa_status_t launch_prefill_fp8_sm103(const Problem &pr, float q_descale, float k
         !encode_tmap_bf16_3d(&to, pr.o, kD, pr.Sq, BH, kBlockM))
         return FA_ERR_CUDA;
     Params p;
-    p.sl2 = static_cast<float>(static_cast<double>(pr.scale) * q_descale * k_descale *
-                               1.4426950408889634);
-    if (!(p.sl2 > 0.0f) || !std::isfinite(p.sl2))
+    // At scale 0 the scores are 0 (zero Q tiles), every weight is 2^kPShift
+    // and the reference settles at 0 on the first visible key.
+    p.zero_q = pr.scale == 0.0f ? 1 : 0;
+    p.sl2 = p.zero_q ? 1.0f
+                     : static_cast<float>(std::fabs(static_cast<double>(pr.scale)) * q_descale *
+                                          k_descale * 1.4426950408889634);
+    if (!std::isfinite(p.sl2))
         return FA_ERR_UNSUPPORTED;
+    p.idesc_qk_neg = std::signbit(pr.scale) ? kIdescNegateA : 0u;
     unsigned grid = 0;
     const fa_status_t st =
         sched::make_schedule(pr, 2.0 * static_cast<double>(pr.Sk) * kD, &p.sc, &grid);

@@ -92,10 +92,21 @@ struct Cfg {
 
 struct Params {
     sched::Schedule sc;  // items and their order (fa_schedule.cuh)
-    float scale;         // softmax scale
-    float scale_log2;    // scale * log2(e)
+    float scale;         // |softmax scale|
+    float scale_log2;    // |scale| * log2(e)
+    // kIdescNegateA when the caller's scale is negative, else 0: the S MMAs
+    // then form -Q K^T, so that scale * Q K^T = |scale| * (-Q K^T) and the
+    // softmax below only ever sees a non-negative scale.
+    uint32_t idesc_qk_neg;
+    // Scale 0 makes every score 0 whatever Q holds: Q tiles are then read
+    // from head index BH, outside the tensor, which TMA fills with zeros, and
+    // the softmax runs with scale_log2 = 1.
+    int zero_q;
     float *lse;
     unsigned int *status;
+    uint64_t wait_ns;   // limit of every bounded wait (kWaitLimitNs unless a test lowers it)
+    int stall_load;     // test only: ring load CTA 0's producer skips (-1: none)
+    __device__ int q_head(int bh) const { return zero_q ? sc.BH : bh; }
 };
 
 // Work-item queue slots. The consumers release a slot when they have finished
@@ -195,8 +206,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_kv = [&](int j, int which, int bh) {
                 const int s = it % C::kStages;
                 const uint32_t use = it / C::kStages;
-                if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status))
+                if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status,
+                                          p.wait_ns))
                     return false;
+                if (it == p.stall_load && blockIdx.x == 0) {
+                    // Test only: this load is never issued, so the MMA thread's
+                    // bounded wait for it runs out and the CTA takes its abort path.
+                    ++it;
+                    return true;
+                }
                 mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
                 const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
                 for (int b = 0; b < C::kBoxes; ++b)
@@ -208,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; ok; ++n) {
                 const int slot = n % kQueue;
                 if (n >= kQueue &&
-                    !mbar_wait(&bars->item_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status))
+                    !mbar_wait(&bars->item_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status, p.wait_ns))
                     break;
                 const int w = sched::grab_item(p.sc);
                 bars->items[slot] = w;
@@ -226,14 +244,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Q_t's buffer is free once the previous item's last MMA on
                     // tile t has completed.
                     if (q_loads[t] > 0 &&
-                        !mbar_wait(&bars->o_done[t], (q_loads[t] - 1) & 1, abort_flag, p.status)) {
+                        !mbar_wait(&bars->o_done[t], (q_loads[t] - 1) & 1, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
                     for (int b = 0; b < C::kBoxes; ++b)
                         tma_load_3d_hint(sQ + t * C::kTileBytes + b * kBoxBytes, &tm_q,
-                                         &bars->q_full[t], b * 64, I.q0[t], I.bh, pol_stream);
+                                         &bars->q_full[t], b * 64, I.q0[t], p.q_head(I.bh),
+                                         pol_stream);
                     ++q_loads[t];
                 }
                 for (int j = 1; j < I.n_kv_max && ok; ++j)
@@ -242,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Drain: every load issued must have landed before the CTA exits.
             for (int t = 0; t < kTiles; ++t)
                 if (q_loads[t] > 0)
-                    mbar_wait_drain(&bars->q_full[t], (q_loads[t] - 1) & 1, p.status);
+                    mbar_wait_drain(&bars->q_full[t], (q_loads[t] - 1) & 1, p.status, p.wait_ns);
             for (int k = max(0, it - C::kStages); k < it; ++k)
-                mbar_wait_drain(&bars->kv_full[k % C::kStages], (k / C::kStages) & 1, p.status);
+                mbar_wait_drain(&bars->kv_full[k % C::kStages], (k / C::kStages) & 1, p.status, p.wait_ns);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -256,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tensor pipe executes one thread's MMAs in order, and the softmax
         // warps have read O_t (epilogue) before they publish the next P_t.
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+            const uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false) | p.idesc_qk_neg;
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
             const uint32_t colS[kTiles] = {C::kColS0, C::kColS1};
             const uint32_t colO[kTiles] = {C::kColO0, C::kColO1};
@@ -286,14 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto ring_wait = [&](int idx) {
                 return mbar_wait(&bars->kv_full[idx % C::kStages], (idx / C::kStages) & 1,
-                                 abort_flag, p.status);
+                                 abort_flag, p.status, p.wait_ns);
             };
             int it = 0;
             uint32_t q_waits[kTiles] = {0, 0}, p_waits[kTiles] = {0, 0};
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 const int slot = n % kQueue;
-                if (!mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status))
+                if (!mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status, p.wait_ns))
                     break;
                 const int w = bars->items[slot];
                 if (w < 0)
@@ -309,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < kTiles && ok; ++t) {
                     if (I.n_kv[t] == 0)
                         continue;
-                    ok = mbar_wait(&bars->q_full[t], (q_waits[t]++) & 1, abort_flag, p.status);
+                    ok = mbar_wait(&bars->q_full[t], (q_waits[t]++) & 1, abort_flag, p.status, p.wait_ns);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
@@ -329,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < kTiles && ok; ++t) {
                         if (j >= I.n_kv[t])
                             continue;
-                        ok = mbar_wait(&bars->p_full[t], (p_waits[t]++) & 1, abort_flag, p.status);
+                        ok = mbar_wait(&bars->p_full[t], (p_waits[t]++) & 1, abort_flag, p.status, p.wait_ns);
                         if (!ok)
                             break;
                         tc_fence_after_sync();
@@ -359,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Drain: all MMAs issued by this thread complete before TMEM is freed.
             umma_commit(&bars->drain);
-            mbar_wait_drain(&bars->drain, 0, p.status);
+            mbar_wait_drain(&bars->drain, 0, p.status, p.wait_ns);
         }
     } else if (warp < kSoftmaxWarps) {
         // ------------------------------------------------------------ softmax warpgroups
@@ -381,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile-uniform here.
             const bool got_item = __all_sync(
                 0xffffffffu,
-                mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status));
+                mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status, p.wait_ns));
             if (named_bar_or(1 + t, 128, !got_item))
                 break;
             const int w = *reinterpret_cast<volatile int *>(&bars->items[slot]);
@@ -398,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = q0 + r;  // query row
             const int lim = visible_keys(i, p.sc.Sq, p.sc.Sk, p.sc.causal);
 
-            // m: the reference max of this row's exponentials (raw score units,
-            // scale > 0). It is updated lazily: only when a tile's max exceeds it
+            // m: the reference max of this row's exponentials (units of the
+            // MMA's scores, whose scale |scale| is >= 0). It is updated lazily: only when a tile's max exceeds it
             // by more than 2^kRescaleLog2 in the exponent (or on the first
             // visible key). O and l always share the same reference, so the
             // result stays exact, and P = 2^((s - m) * sl2) stays <= 2^kRescaleLog2.
@@ -407,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float l = 0.0f;  // running sum of 2^((s - m) * sl2)
             for (int j = 0; j < n_kv && ok; ++j) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], (s_waits++) & 1,
-                                                       abort_flag, p.status));
+                                                       abort_flag, p.status, p.wait_ns));
                 if (!ok)
                     break;
                 tc_fence_after_sync();
@@ -478,11 +497,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // again.
                 float m_use = m, corr = 1.0f;
                 bool any_move = false;  // some lane of the warp moved its reference
+                // A row's first visible key always sets the reference (tested on
+                // m itself: at scale 0 the product (m_new - m) * sl2 is NaN).
                 auto decide = [&](float mx) {
                     const float m_new = fmaxf(m, mx);
-                    const bool move = (m_new - m) * sl2 > kRescaleLog2;
+                    const bool first = m == -INFINITY;
+                    const bool move =
+                        first ? (m_new != -INFINITY) : ((m_new - m) * sl2 > kRescaleLog2);
                     m_use = move ? m_new : m;
-                    corr = move ? ex2_approx((m - m_use) * sl2) : 1.0f;  // 0 when m = -inf
+                    corr = move ? (first ? 0.0f : ex2_approx((m - m_use) * sl2)) : 1.0f;
                     any_move = __any_sync(0xffffffffu, move);
                 };
                 // O_t *= corr after a move (warp-uniform; lanes that did not move
@@ -572,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool got = ok;
             if (got && n_kv > 0) {
                 got = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (o_waits++) & 1,
-                                                        abort_flag, p.status));
+                                                        abort_flag, p.status, p.wait_ns));
                 if (got)
                     tc_fence_after_sync();
             }
@@ -661,10 +684,15 @@ fa_status_t launch(const Problem &pr)
                                                 &p.sc, &grid);
     if (st != FA_OK)
         return st;
-    p.scale = pr.scale;
-    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.scale = fabsf(pr.scale);
+    p.zero_q = pr.scale == 0.0f ? 1 : 0;
+    p.scale_log2 = p.zero_q ? 1.0f : fabsf(pr.scale) * 1.4426950408889634f;
+    p.idesc_qk_neg = std::signbit(pr.scale) ? kIdescNegateA : 0u;
     p.lse = pr.lse;
     p.status = pr.status;
+    p.wait_ns = kWaitLimitNs;
+    p.stall_load = -1;
+    take_stall(kStallPrefill, &p.stall_load, &p.wait_ns);
     auto kern = fa_prefill_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)

@@ -280,8 +280,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr, uint32_t
 // Instruction descriptor for tcgen05.mma .kind::f16 with bf16 A/B and an
 // fp32 accumulator.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format
-//   (1 = bf16); 15 A major (0 = K, 1 = MN); 16 B major; 17-22 N >> 3;
-//   24-28 M >> 4.
+//   (1 = bf16); 13 negate A; 14 negate B; 15 A major (0 = K, 1 = MN);
+//   16 B major; 17-22 N >> 3; 24-28 M >> 4.
+// Bit 13 of either instruction descriptor: the MMA uses -A in place of A
+// (an exact sign flip of every product).
+constexpr uint32_t kIdescNegateA = 1u << 13;
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn_major,
                                                       bool b_mn_major)
 {

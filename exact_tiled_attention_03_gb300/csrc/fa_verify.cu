@@ -64,7 +64,9 @@ struct Params {
     int Sq, Sk, BH, H, n_split;
     int chunk;  // keys per split (multiple of kStageKeys)
     int mode;   // 0: every draft position, 1: causal chain, 2: tree_mask
-    float scale, scale_log2;
+    float scale, scale_log2;     // |scale|, |scale| * log2(e)
+    uint32_t q_sign;             // 0x80008000 for a negative scale (Q enters as -Q), else 0
+    uint32_t q_keep;             // 0 at scale 0 (every score is 0: Q enters as 0), else ~0
     const uint32_t *tree_mask;   // [B, Sq] (mode 2)
     const int32_t *seq_lens;     // [B] keys per sequence (paged); nullptr: Sk for all
     const int32_t *block_table;  // [B, max_pages] physical page of each logical page (paged)
@@ -75,6 +77,8 @@ struct Params {
     float *ws_o;        // [n_split, BH, Sq, D] partial outputs
     float *ws_lse;      // [n_split, BH, Sq]
     unsigned int *status;
+    uint64_t wait_ns;   // limit of every bounded wait (kWaitLimitNs unless a test lowers it)
+    int stall_stage;    // test only: stage CTA (0, 0)'s producer skips (-1: none)
 };
 
 struct Bars {
@@ -235,8 +239,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int s = st % C::kStages;
             const uint32_t use = st / C::kStages;
             if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], (use - 1) & 1,
-                                                               abort_flag, p.status)))
+                                                               abort_flag, p.status, p.wait_ns)))
                 break;
+            if (st == p.stall_stage && split == 0 && bh == 0)
+                continue;  // test only: never issued, so the consumers' bounded wait runs out
             if (lane == 0)
                 mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
             uint8_t *dst = smem + s * C::kStageBytes;
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (lane == 0)
             for (int k = max(0, st - C::kStages); k < st; ++k)
-                mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status);
+                mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status, p.wait_ns);
         // Match the consumers' two block barriers (ring -> scratch, scratch ready).
         __syncthreads();
         __syncthreads();
@@ -302,14 +308,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     const __nv_bfloat16 *qb = p.q + static_cast<size_t>(bh) * p.Sq * D;
 
     // Q as mma A fragments: rows g and g+8, columns kk*16 + 2*tq (+8).
+    // A negative scale enters as -Q (an exact flip of each bf16 sign bit), so
+    // scale * Q K^T = |scale| * (-Q) K^T and the softmax sees |scale| only; at
+    // scale 0 Q enters as 0 and the softmax factor is 1 (every weight 1).
     uint32_t qa[D / 16][4];
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const int c = kk * 16 + 2 * tq;
-        qa[kk][0] = ld_bf16x2_or_zero(qb + g * D + c, g < p.Sq);
-        qa[kk][1] = ld_bf16x2_or_zero(qb + (g + 8) * D + c, g + 8 < p.Sq);
-        qa[kk][2] = ld_bf16x2_or_zero(qb + g * D + c + 8, g < p.Sq);
-        qa[kk][3] = ld_bf16x2_or_zero(qb + (g + 8) * D + c + 8, g + 8 < p.Sq);
+        qa[kk][0] = (ld_bf16x2_or_zero(qb + g * D + c, g < p.Sq) & p.q_keep) ^ p.q_sign;
+        qa[kk][1] = (ld_bf16x2_or_zero(qb + (g + 8) * D + c, g + 8 < p.Sq) & p.q_keep) ^ p.q_sign;
+        qa[kk][2] = (ld_bf16x2_or_zero(qb + g * D + c + 8, g < p.Sq) & p.q_keep) ^ p.q_sign;
+        qa[kk][3] =
+            (ld_bf16x2_or_zero(qb + (g + 8) * D + c + 8, g + 8 < p.Sq) & p.q_keep) ^ p.q_sign;
     }
     const uint32_t rm0 = draft_mask(p, b, g), rm1 = draft_mask(p, b, g + 8);
 
@@ -333,7 +343,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     for (int st = 0; st < n_st && ok; ++st) {
         const int s = st % C::kStages;
-        ok = mbar_wait(&bars->full[s], (st / C::kStages) & 1, abort_flag, p.status);
+        // Warp-uniform outcome: the ldmatrix / mma.sync below need the whole
+        // warp, and after a timeout elsewhere some lanes could give up while
+        // others see the phase complete.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[s], (st / C::kStages) & 1, abort_flag,
+                                               p.status, p.wait_ns));
         if (!ok)
             break;
         const uint32_t sK = smem_a + s * C::kStageBytes;
@@ -373,7 +387,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float mu0 = mn0 == -INFINITY ? 0.0f : mn0;
         const float mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-        const float c0 = ex2_approx((m0 - mu0) * sl2), c1 = ex2_approx((m1 - mu1) * sl2);
+        // 0 while nothing was visible (tested on m itself: at scale 0 the
+        // product (m - mu) * sl2 would be NaN).
+        const float c0 = m0 == -INFINITY ? 0.0f : ex2_approx((m0 - mu0) * sl2);
+        const float c1 = m1 == -INFINITY ? 0.0f : ex2_approx((m1 - mu1) * sl2);
         m0 = mn0;
         m1 = mn1;
         float pr[2][4];
@@ -450,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
                 const float *rw = scr + (w * kMaxRows + row) * kRowStride;
-                const float wt = ex2_approx((rw[D] - M) * sl2);  // 0 for m_w = -inf
+                const float wt = rw[D] == -INFINITY ? 0.0f : ex2_approx((rw[D] - M) * sl2);
                 L += rw[D + 1] * wt;
                 acc += rw[col] * wt;
             }
@@ -543,8 +560,10 @@ fa_status_t launch(const Problem &pr, int n_split, void *ws, size_t ws_bytes,
     p.n_split = n_split;
     p.chunk = static_cast<int>(verify_chunk_keys(pr.Sk, n_split));
     p.mode = opt.tree_mask ? 2 : (pr.causal ? 1 : 0);
-    p.scale = pr.scale;
-    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.scale = fabsf(pr.scale);
+    p.q_keep = pr.scale == 0.0f ? 0u : ~0u;
+    p.scale_log2 = pr.scale == 0.0f ? 1.0f : fabsf(pr.scale) * 1.4426950408889634f;
+    p.q_sign = std::signbit(pr.scale) ? 0x80008000u : 0u;
     p.tree_mask = opt.tree_mask;
     p.seq_lens = opt.seq_lens;
     p.block_table = opt.block_table;
@@ -555,6 +574,9 @@ fa_status_t launch(const Problem &pr, int n_split, void *ws, size_t ws_bytes,
     p.o = static_cast<__nv_bfloat16 *>(pr.o);
     p.lse = pr.lse;
     p.status = pr.status;
+    p.wait_ns = kWaitLimitNs;
+    p.stall_stage = -1;
+    take_stall(kStallVerify, &p.stall_stage, &p.wait_ns);
     p.ws_o = nullptr;
     p.ws_lse = nullptr;
     if (n_split > 1) {

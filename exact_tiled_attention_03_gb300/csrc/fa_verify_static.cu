@@ -14,13 +14,19 @@
 //   * the array is FA_STATIC_SCRATCH_BYTES bytes on every GPU that loads the
 //     library, held until the process exits;
 //   * the first call on a device looks up the array's device address (with
-//     that device current) and caches it; make that first call before any
-//     stream capture;
+//     that device current) and caches it for the calling thread's CUDA
+//     context; make that first call before any stream capture. A call made
+//     in another context (after cudaDeviceReset, or under a driver context
+//     the caller created) looks the address up again;
 //   * every call shares the one array, which keeps the last call's
 //     contents, so calls that overlap on the GPU (other streams, other host
 //     threads) race on it; nothing in it needs to start at zero, because the
 //     split kernel of a call writes every partial its combine reads;
-//   * shapes whose partials do not fit return FA_ERR_WORKSPACE.
+//   * arguments are checked exactly as fa_verify_forward checks them, before
+//     the scratch size; with n_split = 0 the automatic split count is
+//     lowered, if need be, to the largest count whose partials fit (one split
+//     needs no scratch at all); an explicit n_split whose partials do not fit
+//     returns FA_ERR_WORKSPACE.
 #include <mutex>
 
 #include "fa_internal.h"
@@ -33,23 +39,37 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    void *ctx = nullptr;   // context the address was looked up in
+    void *addr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of g_verify_scratch on the current device, looked up once
-// per device with that device current. nullptr on failure.
+// Device address of g_verify_scratch on the current device, looked up with
+// that device current and cached per device for the context it belongs to.
+// nullptr on failure.
 void *scratch_address()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return nullptr;
+    void *ctx = fa::current_context();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr &c = g_scratch[dev];
+    if (!c.addr || ctx != c.ctx) {
         void *p = nullptr;
+        c.addr = nullptr;
         if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr)
             return nullptr;
-        g_scratch_addr[dev] = p;
+        c.addr = p;
+        c.ctx = fa::current_context();  // bound by the lookup if it was not already
     }
-    return g_scratch_addr[dev];
+    return c.addr;
+}
+
+bool fits(int64_t BH, int64_t Sq, int64_t d, int ns)
+{
+    return fa::verify_workspace_bytes(BH, Sq, d, ns) <= size_t(FA_STATIC_SCRATCH_BYTES);
 }
 
 }  // namespace
@@ -59,18 +79,20 @@ extern "C" fa_status_t fa_verify_forward_static(const void *q, const void *k, co
                                                 int64_t Sq, int64_t Sk, int64_t d, int causal,
                                                 float scale, int n_split, void *stream)
 {
-    if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0 || d <= 0 || n_split < 0)
-        return FA_ERR_INVALID_ARG;
-    // An explicit split count is checked against the limit before touching
-    // the device; the automatic one needs the device's SM count.
-    if (n_split > 0 &&
-        fa::verify_workspace_bytes(B * H, Sq, d, n_split) > size_t(FA_STATIC_SCRATCH_BYTES))
-        return FA_ERR_WORKSPACE;
-    const int ns = n_split > 0 ? n_split : fa_verify_auto_splits(B, H, Sq, Sk, d);
-    if (ns <= 0)
-        return FA_ERR_CUDA;
-    if (fa::verify_workspace_bytes(B * H, Sq, d, ns) > size_t(FA_STATIC_SCRATCH_BYTES))
-        return FA_ERR_WORKSPACE;
+    fa_status_t st = fa::verify_check_args(q, k, v, o, lse, B, H, Sq, Sk, d, scale, n_split);
+    if (st != FA_OK)
+        return st;
+    int ns = n_split;
+    if (ns > 0) {
+        if (!fits(B * H, Sq, d, ns))
+            return FA_ERR_WORKSPACE;
+    } else {
+        ns = fa_verify_auto_splits(B, H, Sq, Sk, d);
+        if (ns <= 0)
+            return FA_ERR_CUDA;
+        while (ns > 1 && !fits(B * H, Sq, d, ns))
+            --ns;
+    }
     void *scratch = scratch_address();
     if (!scratch)
         return FA_ERR_CUDA;

@@ -33,7 +33,15 @@
  *             j <= i + (Sk - Sq) (bottom-right alignment: the Sq queries sit
  *             after the first Sk - Sq keys). A row with no visible key gets
  *             O = 0 and LSE = -inf.
- *   Scale     finite and > 0 (normally 1/sqrt(d)).
+ *   Scale     any finite value (normally 1/sqrt(d)); the pages make it a
+ *             plain factor of the scores. Zero gives uniform weights over
+ *             the visible keys (O = their mean, LSE = ln of their count); a
+ *             negative scale favours the least similar keys. The kernels
+ *             form the scores with -Q when scale < 0 (the tensor-core
+ *             operand negation, exact) and run the softmax with |scale|; at
+ *             scale 0 they form them with a zero Q (every score is 0) and a
+ *             softmax factor of 1. The scaled logits are fp32 values, so
+ *             |scale * q . k| must stay within the fp32 range.
  *   Sizes     B, H, Sq, Sk >= 1; d in {64, 128}; Sq, Sk < 2^31; B*H < 2^31.
  *   Pointers  device pointers owned by the caller, 16-byte aligned (the
  *             kernels move tiles with TMA, which needs 16-byte aligned
@@ -61,7 +69,7 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,  /* null pointer, size <= 0, non-finite scale, bad split count */
-    FA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, misaligned pointer, scale <= 0, no sm_103 device */
+    FA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, misaligned pointer, no sm_103 device */
     FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
     FA_ERR_TIMEOUT = 4,      /* a kernel's bounded wait ran out (reported by fa_device_status) */
     FA_ERR_WORKSPACE = 5     /* workspace missing or smaller than fa_workspace_size() */
@@ -71,8 +79,11 @@ typedef enum {
  * Attention forward, dispatching on the shape:
  *   Sq <= FA_VERIFY_MAX_SQ : the split-KV path (fa_verify_forward) with an
  *                            automatic split count; its workspace is taken
- *                            from the stream-ordered allocator
- *                            (cudaMallocAsync / cudaFreeAsync on `stream`);
+ *                            from a library-owned stream-ordered memory pool
+ *                            (cudaMallocFromPoolAsync / cudaFreeAsync on
+ *                            `stream`) that keeps freed blocks for the next
+ *                            call, so it holds the largest workspace a call
+ *                            has needed until the process exits;
  *   otherwise              : the tiled prefill path (fa_prefill_forward),
  *                            which needs no workspace.
  * q, k, v: inputs; o, lse: outputs (every element of both is written).
@@ -144,9 +155,11 @@ fa_status_t fa_prefill_forward(const void *q, const void *k, const void *v, void
  * in fa_forward.
  * d must be 128; q, k, v, o 16-byte aligned, lse 4-byte aligned; any
  * Sq, Sk >= 1. The caller owns every buffer; nothing is allocated.
+ * scale: any finite value, as in fa_forward; the descales must be > 0.
  * Errors: FA_ERR_INVALID_ARG for null pointers, sizes <= 0, a non-finite
- * scale or descale; FA_ERR_UNSUPPORTED for d != 128, a scale or descale <= 0,
- * misaligned pointers or a device other than sm_103.
+ * scale or descale; FA_ERR_UNSUPPORTED for d != 128, a descale <= 0, a
+ * product |scale| * q_descale * k_descale beyond the fp32 range, misaligned
+ * pointers or a device other than sm_103.
  */
 fa_status_t fa_forward_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
                            int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, int causal,
@@ -245,8 +258,8 @@ fa_status_t fa_verify_paged_forward(const void *q, const void *k_pages, const vo
  *   dq        : device bf16 [B, H, Sq, d];  dk, dv: device bf16 [B, H, Sk, d].
  *   workspace : fa_backward_workspace_size() bytes of device memory
  *               (scratch: -D and -LSE * log2(e) per padded query row),
- *               256-byte aligned; NULL takes it from the stream-ordered
- *               allocator on `stream`.
+ *               256-byte aligned; NULL takes it from the library's
+ *               stream-ordered pool on `stream` (as fa_forward does).
  * Enqueues three kernels on `stream`. The third (dQ) is launched with
  * programmatic stream serialization so that it starts on the SMs the second
  * (dK, dV) leaves idle; it waits for the second before completing, so the
@@ -309,14 +322,19 @@ size_t fa_forward_host_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t 
  * passes them only their input and output buffers; serving loops that
  * reserved nearly all of HBM up front; loops that cannot accept the
  * synchronisation an allocation may cause).
- * Arguments, layouts and results are those of fa_verify_forward (n_split = 0
- * picks the automatic count). The split-KV partials go to a file-scope
- * device array of FA_STATIC_SCRATCH_BYTES bytes that every GPU loading the
- * library holds until exit. The first call on a device looks up that
- * array's address with the device current; make it before any stream
- * capture. All calls share the array and it keeps the last call's contents:
- * calls that overlap on the GPU race. Returns FA_ERR_WORKSPACE when the
- * partials (fa_verify_workspace_size) exceed FA_STATIC_SCRATCH_BYTES.
+ * Arguments, layouts, checks and results are those of fa_verify_forward; the
+ * argument checks come first, with the same codes. The split-KV partials go
+ * to a file-scope device array of FA_STATIC_SCRATCH_BYTES bytes that every
+ * GPU loading the library holds until exit. n_split = 0 takes the automatic
+ * count, lowered if need be to the largest count whose partials
+ * (fa_verify_workspace_size) fit in the array; one split needs none, so
+ * every shape fa_verify_forward accepts runs. An explicit n_split whose
+ * partials exceed FA_STATIC_SCRATCH_BYTES returns FA_ERR_WORKSPACE.
+ * The first call on a device looks up the array's address with the device
+ * current; make it before any stream capture. The address is kept for the
+ * calling thread's CUDA context: after cudaDeviceReset (or under another
+ * driver context) the next call looks it up again. All calls share the array
+ * and it keeps the last call's contents: calls that overlap on the GPU race.
  */
 fa_status_t fa_verify_forward_static(const void *q, const void *k, const void *v, void *o,
                                      float *lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,

@@ -97,6 +97,32 @@ fa_status_t fa_selftest_mma_rate(long long *cycles, int mode, int blocks, int it
  */
 fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 
+/*
+ * Makes the next launch of one production kernel stall on purpose, so that
+ * its bounded waits run out and its abort path runs (set the abort flag,
+ * record FA_ERR_TIMEOUT in the device status word, drain the copies and MMAs
+ * in flight, free tensor memory, put the work counter back) without faulting
+ * or hanging the GPU:
+ *   kernel 1  the bf16 prefill kernel (fa_prefill_forward, fa_forward for
+ *             Sq > 16): the first CTA's producer skips its ring load number
+ *             skip_index (K_0, V_0, K_1, V_1, ... counted across its items),
+ *             so the MMA thread's wait for that load runs out;
+ *   kernel 2  the split-KV verify kernel (fa_verify_forward and the entry
+ *             points built on it): the producer of CTA (chunk 0, b*h 0) skips
+ *             its 64-key stage number skip_index, so its consumers' wait runs
+ *             out.
+ * wait_limit_ns becomes the limit of every bounded wait of that launch
+ * (including the drains), in place of the default 2 s. The request is taken
+ * by the next launch of that kernel in this process and then cleared; if the
+ * first CTA issues fewer loads than skip_index + 1, nothing is skipped. Call
+ * fa_device_status() after the stalled launch: it reports FA_ERR_TIMEOUT and
+ * clears the word, which the next launch needs (while the word records a
+ * timeout every launch gives up at its first slow wait).
+ * Returns FA_ERR_INVALID_ARG for another kernel, skip_index < 0, or
+ * wait_limit_ns outside [1 ms, 10 s].
+ */
+fa_status_t fa_testing_stall_next_launch(int kernel, int skip_index, uint64_t wait_limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

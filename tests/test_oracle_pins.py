@@ -112,6 +112,39 @@ def test_zero_query_gives_prefix_means(shape):
         assert np.max(np.abs(lse[:, :, i] - math.log(nv))) < TOL
 
 
+@pytest.mark.parametrize("shape", SHAPES)
+def test_zero_scale_gives_visible_means_for_any_query(shape):
+    """scale = 0 makes every logit 0 whatever Q is (the scale is a plain factor of
+    the scores, Warmup Guide Ch.4): o_i = mean of the visible v_j, lse_i = ln(#visible)."""
+    w, q, k, v = case(*shape, seed=17, factor=4.0)
+    o, lse = oracle.attention(q, k, v, w.causal, 0.0)
+    vd = to_f64(v)
+    for i in range(w.Sq):
+        nv = visible(i, w.Sq, w.Sk, w.causal)
+        if nv == 0:
+            assert np.all(o[:, :, i] == 0) and np.all(np.isneginf(lse[:, :, i]))
+            continue
+        assert np.max(np.abs(o[:, :, i] - vd[:, :, :nv].mean(axis=2))) < TOL
+        assert np.max(np.abs(lse[:, :, i] - math.log(nv))) < TOL
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_negative_scale_equals_the_negated_query(shape):
+    """s_j = scale * (q . k_j) is odd in scale and linear in q, so scale -c on q
+    gives exactly what +c gives on -q (bf16 negation is exact). A kernel that
+    takes |scale| fails this, as does one whose max ignores the sign."""
+    w, q, k, v = case(*shape, seed=19)
+    c = float(np.float32(w.scale))
+    o1, l1 = oracle.attention(q, k, v, w.causal, -c)
+    o2, l2 = oracle.attention(-q, k, v, w.causal, c)
+    o3, l3 = oracle.attention(q, k, v, w.causal, c)
+    assert np.max(np.abs(o1 - o2)) < TOL
+    fin = np.isfinite(l2)
+    assert np.array_equal(np.isfinite(l1), fin)
+    assert np.max(np.abs(l1[fin] - l2[fin]), initial=0.0) < TOL
+    assert np.max(np.abs(o1 - o3)) > 1e-3   # the sign really matters on these inputs
+
+
 @pytest.mark.parametrize("form", [1, 2])
 @pytest.mark.parametrize("causal", [False, True])
 def test_online_forms_equal_two_pass(form, causal):
@@ -260,19 +293,22 @@ def test_matches_independent_numpy_restatement(shape):
     assert np.max(np.abs(lse[fin] - ln[fin]), initial=0.0) < TOL
 
 
+@pytest.mark.parametrize("sign", [1.0, 0.0, -1.0])
 @pytest.mark.parametrize("shape", [s for s in SHAPES if s[2] <= s[3] or not s[5]])
-def test_matches_torch_sdpa_fp64(shape):
+def test_matches_torch_sdpa_fp64(shape, sign):
     """torch.nn.functional.scaled_dot_product_attention (CPU, fp64, math path) with an
-    explicit bottom-right mask; lse from torch.logsumexp of the masked logits."""
+    explicit bottom-right mask; lse from torch.logsumexp of the masked logits. The
+    scale is 1/sqrt(d), 0 or -1/sqrt(d)."""
     w, q, k, v = case(*shape, seed=41)
-    o, lse = oracle.attention(q, k, v, w.causal, w.scale)
+    scale = float(np.float32(w.scale)) * sign
+    o, lse = oracle.attention(q, k, v, w.causal, scale)
     qd, kd, vd = q.double(), k.double(), v.double()
     mask = None
     if w.causal:
         i = torch.arange(w.Sq)[:, None]
         j = torch.arange(w.Sk)[None, :]
         mask = j <= i + (w.Sk - w.Sq)
-    sc = float(np.float32(w.scale))
+    sc = scale
     ot = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, attn_mask=mask, scale=sc)
     logits = sc * (qd @ kd.transpose(-1, -2))
     if mask is not None:
