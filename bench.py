@@ -219,16 +219,22 @@ def time_oracle_sample(w, q, k, v, budget_s: float, seed: int = 7, threads: int 
     enough to occupy every thread (a small probe is dominated by per-call costs
     and would size the sample short), and topped up once if it still ran under
     60 % of the budget."""
+    import numpy as np
     import oracle
 
-    def run(rows):
+    outs = []
+
+    def run(rows, keep=True):
         t0 = time.perf_counter()
-        oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads)
-        return time.perf_counter() - t0
+        res = oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads)
+        dt = time.perf_counter() - t0
+        if keep:
+            outs.append(res)
+        return dt
 
     total = w.B * w.H * w.Sq
     probe = sample_rows(w, n_total=min(64 if threads == 1 else 512, total), seed=seed)
-    per_flop = max(run(probe), 1e-6) / oracle_rows_flops(w, probe)
+    per_flop = max(run(probe, keep=False), 1e-6) / oracle_rows_flops(w, probe)
     avg_row = w.exact_flops() / total
     rows, dt, fl = [], 0.0, 0.0
     for attempt in range(2):
@@ -240,7 +246,32 @@ def time_oracle_sample(w, q, k, v, budget_s: float, seed: int = 7, threads: int 
         if dt >= 0.6 * budget_s or n >= total:
             break
         per_flop = dt / fl
-    return rows, dt, fl
+    o_ref = np.concatenate([np.asarray(a).reshape(-1, w.d) for a, _ in outs])
+    l_ref = np.concatenate([np.asarray(b).reshape(-1) for _, b in outs])
+    return rows, dt, fl, (o_ref, l_ref)
+
+
+TOL = {"o_max_abs": 2e-2, "o_mean_abs": 2e-3, "lse_max_abs": 1e-3}
+
+
+def parity_of_rows(o_dev, lse_dev, rows, ref):
+    """Element-wise errors of the GPU's O and LSE on `rows` against the oracle's
+    values for the same rows (the parity bars of the benchmark spec's tolerance)."""
+    import numpy as np
+
+    o_ref, l_ref = ref
+    idx = torch.tensor(rows, dtype=torch.long, device=o_dev.device)
+    og = o_dev[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
+    lg = lse_dev[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
+    fin = np.isfinite(l_ref)
+    err = np.abs(og - o_ref)
+    lerr = np.abs(lg[fin] - l_ref[fin]) if fin.any() else np.zeros(1)
+    out = {"rows": len(rows), "o_max_abs": float(err.max()), "o_mean_abs": float(err.mean()),
+           "lse_max_abs": float(lerr.max()),
+           "masked_rows_match": bool(np.array_equal(np.isfinite(lg), fin))}
+    out["pass"] = bool(out["masked_rows_match"] and all(out[k] <= v for k, v in TOL.items()))
+    out["tol"] = TOL
+    return out
 
 
 def measure_exp_pipe(w, device, sptr):
@@ -294,7 +325,12 @@ def measure_mma_rate(device, sptr):
 
 
 def run_reference(args, world, rank):
-    """--impl reference: the fp64 CPU oracle on the same workload, rank 0 only."""
+    """--impl reference: the fp64 CPU oracle on the same workload, rank 0 only
+    (under a launcher every rank joins the process group, then the others exit)."""
+    init_dist(world, "gloo")
+    barrier(world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
     if rank != 0:
         return 0
     import oracle
@@ -302,8 +338,9 @@ def run_reference(args, world, rank):
     w = WORKLOADS[args.workload]
     q, k, v = make_qkv(w)
     cores = oracle.max_threads()
-    total_budget = 120.0
-    rows_probe, dt_probe, fl_probe = time_oracle_sample(w, q, k, v, budget_s=2.0)
+    total_budget = args.ref_budget
+    rows_probe, dt_probe, fl_probe, _ = time_oracle_sample(w, q, k, v,
+                                                           budget_s=min(2.0, total_budget / 4))
     per_flop = dt_probe / fl_probe
     avg_row = w.exact_flops() / (w.B * w.H * w.Sq)
     n_rows = int(max(1, total_budget / (args.steps + args.warmup) / (per_flop * avg_row)))
@@ -508,8 +545,8 @@ def main_roofline(w, per_launch_s: float, peaks, n_split: int):
              "peak_source": f"{peaks['source']} bf16 burst",
              "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
              "peak_sustained": peaks["bf16_tflops_sustained"],
-             "kernel": "fa_prefill_kernel<128>",
-             "traffic": ncu_traffic("fa_prefill_kernel<128>", PREFILL_SOURCES, w.name)},
+             "kernel": f"fa_prefill_kernel<{w.d}>",
+             "traffic": ncu_traffic(f"fa_prefill_kernel<{w.d}>", PREFILL_SOURCES, w.name)},
             1)
 
 
@@ -567,6 +604,27 @@ def run_ours(args, world, rank, local):
           if 0 < w.Sq <= _capi.FA_VERIFY_MAX_SQ else 0)
     roofline, launches_per_step = main_roofline(w, per_launch_s, peaks, ns)
 
+    # the same step back to back for >= --sustained-s of device time, with its
+    # own clock record: the steady state (power cap) next to the burst above
+    sustained = None
+    if args.sustained_s > 0:
+        n_sus = max(args.steps, int(args.sustained_s / per_launch_s) + 1)
+        with ClockSampler(local) as clk2:
+            barrier(world)
+            torch.cuda.synchronize()
+            t0s = clk2.mark()
+            ds = time_steps(step, n_sus, stream)
+            t1s = clk2.mark()
+            barrier(world)
+        fa.check(fa.fa_device_status(sptr), "device status after sustained region")
+        ds_max = reduce_max(ds, world, device)
+        v_sus = reduce_sum(float(w.exact_flops() * n_sus), world, device) / ds_max / 1e12
+        r_sus = main_roofline(w, ds / n_sus, peaks, ns)[0]
+        sustained = {"value": v_sus, "unit": "TFLOP/s", "steps": n_sus, "device_s": ds_max,
+                     "ms_per_step": 1e3 * ds_max / n_sus, "roofline_frac": r_sus["frac"],
+                     "roofline_frac_sustained_peak": r_sus.get("frac_sustained"),
+                     "clocks": clk2.summary(t0s, t1s)}
+
     # end to end through the C ABI call that takes host buffers (fa_forward_host):
     # pinned host inputs and outputs, every step's host-to-device and
     # device-to-host copies inside the timed region (pipelined by the call)
@@ -599,6 +657,7 @@ def run_ours(args, world, rank, local):
 
     # the decode-shaped verify path, against the HBM roofline
     verify = None
+    verify_keep = None
     if not args.no_verify:
         wv = rank_workload(VERIFY, rank)
         qv, kv_, vv = (t.to(device) for t in make_qkv(wv))
@@ -614,19 +673,34 @@ def run_ours(args, world, rank, local):
             if st != 0:
                 raise _capi.FAError(st, "fa_verify_forward")
 
-        for _ in range(args.warmup):
-            vstep()
-        n_v = max(10, args.steps)
-        dv = time_steps(vstep, n_v, stream)
+        def fstep():  # the main entry point: its own stream-ordered workspace
+            st = _capi.fa_forward(qv, kv_, vv, ov, lv, wv.B, wv.H, wv.Sq, wv.Sk, wv.d, wv.causal,
+                                  wv.scale, sptr)
+            if st != 0:
+                raise _capi.FAError(st, "fa_forward")
+
+        n_v = max(200, args.steps)
+        res = {}
+        for name, fn in (("fa_forward", fstep), ("fa_verify_forward", vstep)):
+            for _ in range(args.warmup):
+                fn()
+            res[name] = time_steps(fn, n_v, stream) / n_v
         fa.check(fa.fa_device_status(sptr), "device status after verify")
-        per = dv / n_v
+        per = res["fa_verify_forward"]
         gbs = wv.io_bytes() / per / 1e9
+        gbs_f = wv.io_bytes() / res["fa_forward"] / 1e9
         verify = {"workload": wv.name, "us_per_step": per * 1e6, "GB/s": gbs,
                   "hbm_peak_GB/s": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
-                  "bytes_per_step": wv.io_bytes(), "n_split": n_split,
+                  "bytes_per_step": wv.io_bytes(), "n_split": n_split, "steps": n_v,
                   "launches_per_step": 1 if n_split == 1 else 2,
+                  "via_fa_forward": {"us_per_step": res["fa_forward"] * 1e6, "GB/s": gbs_f,
+                                     "frac": gbs_f / peaks["hbm_gbs"],
+                                     "workspace": "library pool, stream-ordered"},
                   "traffic": ncu_traffic("fa_verify_split_kernel", VERIFY_SOURCES, wv.name)}
-        del qv, kv_, vv, ov, lv, ws
+        del ws
+        if rank == 0 and world == 1 and not args.no_cpu:
+            verify_keep = (wv, tuple(t.cpu() for t in (qv, kv_, vv)), ov, lv)
+        del qv, kv_, vv
 
     # the backward pass on the same workload (dQ, dK, dV by recomputation from
     # LSE); algorithmic FLOPs: 5 GEMMs of 2*d per visible pair = 2.5x forward
@@ -652,14 +726,17 @@ def run_ours(args, world, rank, local):
         verify_ext = measure_verify_variants(rank_workload(VERIFY, rank), device, sptr, args,
                                              peaks)
 
-    # the CPU oracle on a bounded sample (rank 0, N = 1 only)
+    # the CPU oracle on a bounded sample (rank 0, N = 1 only); the same rows
+    # give the parity of the GPU outputs against the oracle
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
 
         cores = oracle.max_threads()
-        rows, dtc, flc = time_oracle_sample(w, q_h, k_h, v_h, budget_s=args.cpu_budget)
-        rows1, dt1, fl1 = time_oracle_sample(w, q_h, k_h, v_h, budget_s=2.0, seed=11, threads=1)
+        rows, dtc, flc, ref = time_oracle_sample(w, q_h, k_h, v_h, budget_s=args.cpu_budget)
+        rows1, dt1, fl1, _ = time_oracle_sample(w, q_h, k_h, v_h, budget_s=2.0, seed=11,
+                                                threads=1)
         cpu = {"value": flc / dtc / 1e12, "unit": "TFLOP/s", "cores": cores,
                "kind": "oracle",
                "sample": f"{len(rows)} seeded query rows of {w.name} "
@@ -669,6 +746,15 @@ def run_ours(args, world, rank, local):
                "affinity_cpus": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None,
                "omp_num_threads": os.environ.get("OMP_NUM_THREADS"),
                "full_size_s_extrapolated": w.exact_flops() / (flc / dtc)}
+        # the GPU's O and LSE on the rows the oracle just computed
+        parity = {w.name: parity_of_rows(o, lse, rows, ref)}
+        if verify_keep is not None:
+            wv, (qv_h, kv_h, vv_h), ov, lv = verify_keep
+            rv, dtv, flv, refv = time_oracle_sample(wv, qv_h, kv_h, vv_h, budget_s=3.0, seed=13)
+            parity[wv.name] = parity_of_rows(ov, lv, rv, refv)
+            cpu["verify"] = {"value": wv.io_bytes() * (flv / wv.exact_flops()) / dtv / 1e9,
+                             "unit": "GB/s", "sample": f"{len(rv)} seeded query rows of "
+                             f"{wv.name} ({dtv:.1f} s)"}
 
     if rank == 0:
         line = {
@@ -681,7 +767,7 @@ def run_ours(args, world, rank, local):
             "fa_convention_tflops": w.fa_convention_flops() * args.steps * world / dt_max / 1e12,
             "e2e": e2e, "verify": verify, "verify_variants": verify_ext, "backward": backward,
             "fp8": fp8, "forward_other": forward_other, "exp_pipe": exp_pipe, "mma_rate": mma_rate,
-            "cpu_baseline": cpu,
+            "cpu_baseline": cpu, "parity": parity, "sustained": sustained,
             "clocks": clocks,
             "gpu_launches": args.steps * launches_per_step,
             "gpu": torch.cuda.get_device_name(device),
@@ -692,7 +778,27 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def launch_command(argv, n: int, port: int):
+    """The torchrun command that runs this script as `n` ranks on this node
+    (one process per GPU, rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+            os.path.abspath(__file__)] + list(argv)
+
+
+def launch_ranks(argv, n: int) -> int:
+    """`bench.py --gpus N` started without a launcher: start N ranks under
+    torchrun and return their exit status (rank 0 prints the line)."""
+    import socket
+
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    return subprocess.run(launch_command(argv, n, port)).returncode
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
@@ -705,10 +811,20 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=120.0,
+                    help="--impl reference: seconds of oracle time for the whole run")
+    ap.add_argument("--sustained-s", type=float, default=1.5,
+                    help="device seconds of back-to-back steps for the sustained record (0: off)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return launch_ranks(argv, args.gpus)
     world, rank, local = dist_env()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but the launcher started {world} ranks")
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_ours(args, world, rank, local)

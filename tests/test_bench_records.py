@@ -69,3 +69,7 @@ def test_main_roofline_follows_the_kernel_fa_forward_dispatches_to():
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and launches == 1
     assert abs(r["achieved"] - wp.exact_flops() / 1e-3 / 1e12) < 1e-9
     assert r["traffic"] is None  # the committed capture is of another workload
+    wl = WORKLOADS["prefill_b1h32s32768d64_causal"]
+    r, launches = bench.main_roofline(wl, 1e-3, peaks, 0)
+    assert r["bound"] == "tensor" and r["kernel"] == "fa_prefill_kernel<64>" and launches == 1
+    assert r["traffic"] is None  # no record for the d = 64 kernel

@@ -111,3 +111,39 @@ def test_split_kv_exchange_across_two_gloo_ranks():
     for rank in (0, 1):
         err_o, err_l = out[rank]
         assert err_o < 1e-12 and err_l < 1e-12
+
+
+def test_bench_launches_its_own_ranks_when_started_without_a_launcher(capfd, monkeypatch):
+    """`bench.py --gpus 2` with no WORLD_SIZE in the environment starts two
+    ranks under torchrun itself (rendezvous on 127.0.0.1). The reference arm
+    runs on host cores, so the launch, the rendezvous of both ranks and rank
+    0's single JSON line are exercised without a GPU."""
+    import json
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        monkeypatch.delenv(var, raising=False)
+    cmd = bench.launch_command(["--gpus", "2"], 2, 12345)
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"]
+    assert "--nproc-per-node=2" in cmd and "127.0.0.1" in cmd
+    rc = bench.main(["--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3",
+                     "--workload", "tiny_b1h1s256d64_causal", "--ref-budget", "2"])
+    assert rc == 0
+    lines = [l for l in capfd.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, lines       # rank 0 alone prints
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["steps"] == 2
+    assert rec["value"] > 0 and rec["config"]["workload"] == "tiny_b1h1s256d64_causal"
+
+
+def test_bench_refuses_a_rank_count_other_than_its_launcher(monkeypatch):
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "2", "--impl", "reference"])
