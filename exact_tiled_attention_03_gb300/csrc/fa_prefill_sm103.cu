@@ -67,6 +67,10 @@ constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (1
 // Lazy rescale threshold, in log2 units of the exponent (factor 256).
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kRescaleFactor = 256.0f;  // 2^kRescaleLog2
+// Largest move of the reference made by shifting the p already computed
+// (2^kShiftLog2 stays far inside fp32 and bf16 range); larger jumps recompute.
+constexpr float kShiftLog2 = 100.0f;
+constexpr float kShiftLimit = 1.2676506e30f;  // 2^kShiftLog2
 
 template <int D>
 struct Cfg {
@@ -417,13 +421,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = q0 + r;  // query row
             const int lim = visible_keys(i, p.sc.Sq, p.sc.Sk, p.sc.causal);
 
-            // m: the reference max of this row's exponentials (units of the
-            // MMA's scores, whose scale |scale| is >= 0). It is updated lazily: only when a tile's max exceeds it
-            // by more than 2^kRescaleLog2 in the exponent (or on the first
-            // visible key). O and l always share the same reference, so the
-            // result stays exact, and P = 2^((s - m) * sl2) stays <= 2^kRescaleLog2.
-            float m = -INFINITY;
-            float l = 0.0f;  // running sum of 2^((s - m) * sl2)
+            // ref: the reference of this row's exponentials, in log2 units of
+            // the exponent (p = 2^(s * sl2 - ref), s the MMA's score). It is
+            // set by the row's first visible tile to that tile's max and moved
+            // only when a tile's p would exceed 2^kRescaleLog2: by an integer
+            // k, multiplying the p already computed (bf16) and O, l by 2^-k,
+            // all exact. O and l always share the reference, so the result
+            // stays exact, and P stays <= 2^kRescaleLog2.
+            float ref = -INFINITY;
+            float l = 0.0f;  // running sum of 2^(s * sl2 - ref), fp32 (for the LSE)
+            // O's divisor: l, except that a tile whose reference moved in place
+            // adds the sum of its bf16 weights (those P V used), so that a row's
+            // dominant weight, rounded to bf16 there, cancels in O / ln.
+            float ln = 0.0f;
             for (int j = 0; j < n_kv && ok; ++j) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], (s_waits++) & 1,
                                                        abort_flag, p.status, p.wait_ns));
@@ -495,18 +505,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // 2^kRescaleLog2. NaN (both -inf) compares false: nothing visible
                 // yet, keep m. Until P is written, S_t is intact and may be read
                 // again.
-                float m_use = m, corr = 1.0f;
+                float ref_use = ref, corr = 1.0f;
                 bool any_move = false;  // some lane of the warp moved its reference
-                // A row's first visible key always sets the reference (tested on
-                // m itself: at scale 0 the product (m_new - m) * sl2 is NaN).
+                float norm_sum = -1.0f;  // >= 0: this tile's contribution to ln (else the fp32 sum)
+                // From the tile's max score mx: a row's first visible key sets the
+                // reference to the max (tested on ref itself: at scale 0 a product
+                // with sl2 would be NaN); later the reference moves to the max
+                // when it lies more than 2^kRescaleLog2 above it.
                 auto decide = [&](float mx) {
-                    const float m_new = fmaxf(m, mx);
-                    const bool first = m == -INFINITY;
+                    const float x_max = mx * sl2;
+                    const bool first = ref == -INFINITY;
                     const bool move =
-                        first ? (m_new != -INFINITY) : ((m_new - m) * sl2 > kRescaleLog2);
-                    m_use = move ? m_new : m;
-                    corr = move ? (first ? 0.0f : ex2_approx((m - m_use) * sl2)) : 1.0f;
+                        first ? (mx != -INFINITY) : (x_max - ref > kRescaleLog2);
+                    ref_use = move ? x_max : ref;
+                    corr = move ? (first ? 0.0f : ex2_approx(ref - ref_use)) : 1.0f;
                     any_move = __any_sync(0xffffffffu, move);
+                };
+                // Moves the reference up by the integer k >= 0 (per lane): the p
+                // already in pk (bf16) and acc (fp32) are multiplied by 2^-k, and
+                // corr = 2^-k takes O and l along. A product with a power of two
+                // is exact; only weights below 2^-126 of the new reference round
+                // (to a subnormal or 0). The same as recomputing p against
+                // ref + k, without another pass over S.
+                auto shift = [&](int k) {
+                    const float f = __int_as_float((127 - k) << 23);
+                    const uint32_t h = static_cast<uint32_t>(127 - k) << 7;
+                    const uint32_t f2 = h | (h << 16);
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 2; ++c)
+                        pk[c] = mul_bf16x2(pk[c], f2);
+                    const float2 fx2 = make_float2(f, f);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        acc[q] = fmul2(acc[q], fx2);
+                    ref_use = ref + static_cast<float>(k);
+                    corr = f;
+                    if (k > 0)
+                        norm_sum = sum_bf16x2_row(pk);
                 };
                 // O_t *= corr after a move (warp-uniform; lanes that did not move
                 // multiply by 1). PV_t(j-1) has completed: S_t(j), committed after
@@ -534,22 +569,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Speculative pass without the max: when every lane has a
                     // reference, p is computed against it. Every p is >= 0, so a row
                     // sum of at most 2^kRescaleLog2 shows that no p exceeds
-                    // 2^kRescaleLog2 and m stays; a larger sum sends the warp to the
-                    // max pass and then to the exponentials against m_use. The
-                    // passes run one per iteration of this loop, so the code holds
-                    // one copy of the pass (three copies spilled at 168 registers).
-                    // Stages: 0 speculative exponentials, 1 max, 2 exponentials.
-                    int stage = __all_sync(0xffffffffu, m != -INFINITY) ? 0 : 1;
+                    // 2^kRescaleLog2 and the reference stays. A larger sum (up to
+                    // 2^kShiftLimit, so that no p can have overflowed) is settled
+                    // from the packed p: their max, and a shift by its exponent when
+                    // it exceeds 2^kRescaleLog2. Only a larger sum, or a row's first
+                    // tile, runs the max pass and then the exponentials against the
+                    // new reference. The passes run one per iteration of this loop,
+                    // so the code holds one copy of the pass (three copies spilled
+                    // at 168 registers). Stages: 0 speculative exponentials, 1 max,
+                    // 2 exponentials.
+                    int stage = __all_sync(0xffffffffu, ref != -INFINITY) ? 0 : 1;
 #pragma unroll 1
                     while (true) {
                         const bool with_exp = stage != 1;
                         const float neg =
-                            stage == 0 ? -m * sl2 : ((m_use == -INFINITY) ? 0.0f : -m_use * sl2);
+                            stage == 0 ? -ref : ((ref_use == -INFINITY) ? 0.0f : -ref_use);
                         const float mx = pass(with_exp, !with_exp, neg);
                         if (stage == 0) {
                             const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-                            if (!__any_sync(0xffffffffu, a.x + a.y > kRescaleFactor))
+                            const float sum = a.x + a.y;
+                            if (!__any_sync(0xffffffffu, sum > kRescaleFactor))
                                 break;
+                            if (__all_sync(0xffffffffu, sum <= kShiftLimit)) {
+                                const float pmax = max_bf16x2_row(pk);
+                                const int k =
+                                    pmax > kRescaleFactor ? (__float_as_int(pmax) >> 23) - 127 : 0;
+                                any_move = __any_sync(0xffffffffu, k > 0);
+                                if (any_move) {
+                                    shift(k);
+                                    rescale_o();
+                                }
+                                break;
+                            }
                             stage = 1;
                         } else if (stage == 1) {
                             decide(mx);
@@ -561,13 +612,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     // d = 64: the speculative pass finds the tile's max while it
-                    // computes p against m (the form above measured 1.01x to 1.07x
-                    // slower at this head dim); a second pass follows when m moves.
-                    const bool spec = __all_sync(0xffffffffu, m != -INFINITY);
-                    decide(pass(spec, true, spec ? -m * sl2 : 0.0f));
-                    if (!spec || any_move) {
-                        pass(true, true, (m_use == -INFINITY) ? 0.0f : -m_use * sl2);
-                        rescale_o();
+                    // computes p against the reference (the form above measured
+                    // 1.01x to 1.07x slower at this head dim). A move up to
+                    // kShiftLimit above the reference shifts the p in place by the
+                    // integer ceil(x_max - ref); a row's first tile, or a larger
+                    // jump, runs a second pass against the new reference.
+                    const bool spec = __all_sync(0xffffffffu, ref != -INFINITY);
+                    const float mx = pass(spec, true, spec ? -ref : 0.0f);
+                    const float delta = mx * sl2 - ref;  // -inf for a row with nothing visible
+                    if (spec && __all_sync(0xffffffffu, !(delta > kShiftLog2))) {
+                        const bool move = delta > kRescaleLog2;
+                        any_move = __any_sync(0xffffffffu, move);
+                        if (any_move) {
+                            shift(move ? static_cast<int>(ceilf(delta)) : 0);
+                            rescale_o();
+                        }
+                    } else {
+                        decide(mx);
+                        if (!spec || any_move) {
+                            pass(true, true, (ref_use == -INFINITY) ? 0.0f : -ref_use);
+                            rescale_o();
+                        }
                     }
                 }
                 // P (bf16 pairs) over S_t's first 64 columns, then publish.
@@ -580,7 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
                 const float2 a = fadd2(a01, a23);
                 l = l * corr + (a.x + a.y);
-                m = m_use;
+                ln = ln * corr + (norm_sum >= 0.0f ? norm_sum : a.x + a.y);
+                ref = ref_use;
             }
 
             // -------------------------------------------------------- epilogue
@@ -604,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+            const float inv_l = (ln > 0.0f) ? 1.0f / ln : 0.0f;
             uint8_t *sOut = smem + C::kOffOut + t * kBoxBytes;
             const uint32_t sOut_a = smem_u32(sOut);
 #pragma unroll
@@ -645,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (i < p.sc.Sq) {
-                const float lse = (l > 0.0f) ? m * p.scale + logf(l) : -INFINITY;
+                // ref is in log2 units: ref * ln 2 is the max in units of the
+                // scaled scores
+                const float lse = (l > 0.0f) ? ref * 0.69314718055994531f + logf(l) : -INFINITY;
                 p.lse[static_cast<size_t>(I.bh) * p.sc.Sq + i] = lse;
             }
             release();

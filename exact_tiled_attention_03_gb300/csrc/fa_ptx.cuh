@@ -562,6 +562,45 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return d;
 }
 
+// a * b on two bf16 lanes, rounded once (a product with a power of two is exact
+// while it stays a normal number).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0u));
+    return d;
+}
+
+// Largest of the 2 * N bf16 values packed in v (non-NaN), as fp32.
+template <int N>
+__device__ __forceinline__ float max_bf16x2_row(const uint32_t (&v)[N])
+{
+    uint32_t t[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i)
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(t[i]) : "r"(v[2 * i]), "r"(v[2 * i + 1]));
+#pragma unroll
+    for (int w = N / 4; w >= 1; w /= 2)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(t[i]) : "r"(t[i]), "r"(t[i + w]));
+    return fmaxf(__uint_as_float(t[0] << 16), __uint_as_float(t[0] & 0xFFFF0000u));
+}
+
+// Sum of the 2 * N bf16 values packed in v, in fp32.
+template <int N>
+__device__ __forceinline__ float sum_bf16x2_row(const uint32_t (&v)[N])
+{
+    float2 a[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        a[i % 4] = fadd2(a[i % 4], make_float2(__uint_as_float(v[i] << 16),
+                                               __uint_as_float(v[i] & 0xFFFF0000u)));
+    const float2 t = fadd2(fadd2(a[0], a[1]), fadd2(a[2], a[3]));
+    return t.x + t.y;
+}
+
 __device__ __forceinline__ void tmem_st_wait()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
