@@ -613,26 +613,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // d = 64: the speculative pass finds the tile's max while it
                     // computes p against the reference (the form above measured
-                    // 1.01x to 1.07x slower at this head dim). A move up to
-                    // kShiftLimit above the reference shifts the p in place by the
-                    // integer ceil(x_max - ref); a row's first tile, or a larger
-                    // jump, runs a second pass against the new reference.
+                    // 1.01x to 1.07x slower at this head dim); a second pass
+                    // follows when the reference moves (a shift in place of it
+                    // measured 1.015x slower here).
                     const bool spec = __all_sync(0xffffffffu, ref != -INFINITY);
-                    const float mx = pass(spec, true, spec ? -ref : 0.0f);
-                    const float delta = mx * sl2 - ref;  // -inf for a row with nothing visible
-                    if (spec && __all_sync(0xffffffffu, !(delta > kShiftLog2))) {
-                        const bool move = delta > kRescaleLog2;
-                        any_move = __any_sync(0xffffffffu, move);
-                        if (any_move) {
-                            shift(move ? static_cast<int>(ceilf(delta)) : 0);
-                            rescale_o();
-                        }
-                    } else {
-                        decide(mx);
-                        if (!spec || any_move) {
-                            pass(true, true, (ref_use == -INFINITY) ? 0.0f : -ref_use);
-                            rescale_o();
-                        }
+                    decide(pass(spec, true, spec ? -ref : 0.0f));
+                    if (!spec || any_move) {
+                        pass(true, true, (ref_use == -INFINITY) ? 0.0f : -ref_use);
+                        rescale_o();
                     }
                 }
                 // P (bf16 pairs) over S_t's first 64 columns, then publish.
