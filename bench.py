@@ -304,12 +304,14 @@ def measure_exp_pipe(w, device, sptr):
             "tensor_ms_lower_bound": w.exact_flops() / 1917.5e12 * 1e3}
 
 
-MMA_FORMS = {0: "ss_n128", 1: "ss_2x_n64", 2: "ts_n128", 3: "ts_2x_n64", 4: "ss_n256"}
+MMA_FORMS = {0: "ss_n128", 1: "ss_2x_n64", 2: "ts_n128", 3: "ts_2x_n64", 4: "ss_n256",
+             5: "e4m3_ss_n128", 6: "e4m3_ts_n128"}
 
 
 def measure_mma_rate(device, sptr):
-    """SM cycles per 128 x 128 x 128 bf16 tcgen05 product in each operand form
-    (one CTA per SM, median over CTAs). 512 is the nominal dense rate."""
+    """SM cycles per 128 x 128 x 128 tcgen05 product in each operand form (bf16,
+    and E4M3 with .kind::f8f6f4), one CTA per SM, median over CTAs. 512 is the
+    nominal dense bf16 rate."""
     from exact_tiled_attention_03_gb300 import _capi
 
     sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -321,7 +323,8 @@ def measure_mma_rate(device, sptr):
         torch.cuda.synchronize(device)
         per = cyc.double().median().item() / (iters * (2 if mode == 4 else 1))
         out[name] = round(per, 1)
-    return {"clk_per_128x128x128": out, "nominal": 512}
+    return {"clk_per_128x128x128": out, "nominal": 512,
+            "e4m3_over_bf16_rate": out["ss_n128"] / out["e4m3_ss_n128"]}
 
 
 def run_reference(args, world, rank):
@@ -437,10 +440,11 @@ def measure_other_forward(device, sptr, args, peaks):
     return out
 
 
-def measure_fp8(w, device, sptr, args, peaks):
+def measure_fp8(w, device, sptr, args, peaks, mma_rate):
     """The FP8 forward (E4M3 Q, K, V with per-tensor descales, bf16 O) on the same
     workload and algorithmic FLOPs, against the FP8 dense peak: the measured
-    bf16 burst peak times the nominal FP8/bf16 tensor ratio of 2."""
+    bf16 burst peak times the measured ratio of the tcgen05 rates (cycles per
+    128 x 128 x 128 product, bf16 over E4M3, both operands from shared memory)."""
     from exact_tiled_attention_03_gb300 import _capi
     from exact_tiled_attention_03_gb300.inputs import make_qkv_fp8
 
@@ -461,9 +465,12 @@ def measure_fp8(w, device, sptr, args, peaks):
     per = time_steps(step, n, torch.cuda.current_stream(device)) / n
     _capi.check(_capi.fa_device_status(sptr), "device status after fp8")
     tf = w.exact_flops() / per / 1e12
-    peak = 2.0 * peaks["bf16_tflops"]
+    ratio = mma_rate["e4m3_over_bf16_rate"]
+    peak = ratio * peaks["bf16_tflops"]
     return {"workload": w.name, "ms_per_step": per * 1e3, "TFLOP/s": tf, "peak": peak,
-            "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)",
+            "peak_source": f"{peaks['source']} bf16 burst x {ratio:.3f}, the measured "
+                           "e4m3/bf16 rate ratio (tcgen05 kind::f8f6f4 microbenchmark)",
+            "frac_of_nominal_2x": tf / (2.0 * peaks["bf16_tflops"]),
             "frac": tf / peak, "dtype": "e4m3 in, fp32 accumulate, bf16 out",
             "launches_per_step": 1,
             "traffic": ncu_traffic("fa_prefill_fp8_kernel", FP8_SOURCES, w.name)}
@@ -708,17 +715,18 @@ def run_ours(args, world, rank, local):
     if not args.no_backward:
         backward = measure_backward(w, device, sptr, args, peaks)
 
+    # the tensor-pipe rates (bf16 and E4M3 forms) and the exp-pipe bound of the
+    # prefill step (microbenchmarks)
+    mma_rate = measure_mma_rate(device, sptr)
+    exp_pipe = measure_exp_pipe(w, device, sptr)
+
     # the FP8 forward on the same workload
     fp8 = None
     if not args.no_fp8:
-        fp8 = measure_fp8(w, device, sptr, args, peaks)
+        fp8 = measure_fp8(w, device, sptr, args, peaks, mma_rate)
 
     # the other prefill configurations
     forward_other = measure_other_forward(device, sptr, args, peaks)
-
-    # the exp-pipe bound of the prefill step (MUFU microbenchmark)
-    exp_pipe = measure_exp_pipe(w, device, sptr)
-    mma_rate = measure_mma_rate(device, sptr)
 
     # the verify step's tree-mask and paged-cache forms, same bytes and roofline
     verify_ext = None

@@ -861,7 +861,7 @@ fa_status_t fa_selftest_mma_rate(long long *cycles, int mode, int blocks, int it
 {
     if (!cycles || blocks <= 0 || iters <= 0)
         return FA_ERR_INVALID_ARG;
-    if (mode < 0 || mode > 4)
+    if (mode < 0 || mode > 6)
         return FA_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(cycles) % alignof(long long) != 0)
         return FA_ERR_UNSUPPORTED;

@@ -9,8 +9,9 @@
 //  * fa_selftest_umma_f8_kernel: the E4M3 products of the FP8 forward (A from
 //    shared or tensor memory, B K-major or MN-major).
 //  * fa_selftest_mufu_kernel: exp2 (MUFU) throughput, the softmax's second bound.
-//  * fa_selftest_mma_rate_kernel: cycles per bf16 tcgen05.mma for the operand
-//    shapes the kernels choose between (N = 64 / 128 / 256, A from shared or
+//  * fa_selftest_mma_rate_kernel: cycles per tcgen05.mma product for the
+//    operand shapes the kernels choose between (bf16 with N = 64 / 128 / 256,
+//    A from shared or tensor memory; E4M3 with N = 128, A from shared or
 //    tensor memory).
 //  * fa_selftest_wait_kernel: the bounded mbarrier wait of the attention
 //    kernels on a barrier that nothing completes; it must give up after the
@@ -387,12 +388,27 @@ __global__ void __launch_bounds__(128, 1)
                     for (int kk = 0; kk < 8; ++kk)
                         umma_bf16_ts(tmem + 256 + 64 * h, tmem + kk * 8,
                                      b0 + koff(kk, 16384) + ((8192 * h) >> 4), i64, kk > 0);
-        } else if (ok) {
+        } else if (ok && mode == 4) {
             for (int it = 0; it < iters; ++it)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     umma_bf16_ss(tmem + 256, a0 + koff(kk, 16384), b0 + koff(kk, 32768), i256,
                                  kk > 0);
+        } else if (ok && mode == 5) {
+            // E4M3 A and B from shared memory: a 128-byte row holds all 128 K
+            // elements, and a K = 32 step moves 32 bytes along it.
+            constexpr uint32_t if8 = idesc_e4m3_f32(128, 128, false, false);
+            for (int it = 0; it < iters; ++it)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_f8_ss(tmem + 256, a0 + 2 * kk, b0 + 2 * kk, if8, kk > 0);
+        } else if (ok) {
+            // E4M3 A from tensor memory (four per column: 8 columns per K = 32)
+            constexpr uint32_t if8 = idesc_e4m3_f32(128, 128, false, false);
+            for (int it = 0; it < iters; ++it)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_f8_ts(tmem + 256, tmem + kk * 8, b0 + 2 * kk, if8, kk > 0);
         }
         umma_commit(bar);
         ok = ok && mbar_wait_drain(bar, 1, status);

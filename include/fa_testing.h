@@ -69,16 +69,19 @@ fa_status_t fa_selftest_umma_f8(const void *a, const void *b, float *c, int n, i
 fa_status_t fa_selftest_mufu(float *out, int blocks, int iters, void *stream);
 
 /*
- * tcgen05.mma rate microbenchmark (bf16 operands, fp32 accumulator, M = 128):
- * `blocks` CTAs (one per SM at most is meaningful; each holds 97 KB of shared
- * memory and all 512 TMEM columns), one thread each issuing `iters` rounds of
- * one 128 x 128 x 128 product as 8 instructions of K = 16, in form `mode`:
- *   0  A and B from shared memory, N = 128
- *   1  A and B from shared memory, two N = 64 halves (each 8 back-to-back
- *      MMAs into its own accumulator)
- *   2  A from tensor memory, N = 128
- *   3  A from tensor memory, two N = 64 halves
- *   4  A and B from shared memory, N = 256 (a round is two products)
+ * tcgen05.mma rate microbenchmark (fp32 accumulator, M = 128): `blocks` CTAs
+ * (one per SM at most is meaningful; each holds 97 KB of shared memory and all
+ * 512 TMEM columns), one thread each issuing `iters` rounds of one
+ * 128 x 128 x 128 product, in form `mode`:
+ *   0  bf16, A and B from shared memory, N = 128 (8 instructions of K = 16)
+ *   1  bf16, A and B from shared memory, two N = 64 halves (each 8
+ *      back-to-back MMAs into its own accumulator)
+ *   2  bf16, A from tensor memory, N = 128
+ *   3  bf16, A from tensor memory, two N = 64 halves
+ *   4  bf16, A and B from shared memory, N = 256 (a round is two products)
+ *   5  E4M3 (.kind::f8f6f4), A and B from shared memory, N = 128
+ *      (4 instructions of K = 32)
+ *   6  E4M3, A from tensor memory, N = 128
  * cycles[b] (device memory, `blocks` entries) receives the SM clock cycles of
  * CTA b from its first issue to the completion of its last MMA, or -1 if the
  * bounded wait for completion gave up (the device status word then records
