@@ -726,7 +726,7 @@ def run_ours(args, world, rank, local):
         fp8 = measure_fp8(w, device, sptr, args, peaks, mma_rate)
 
     # the other prefill configurations
-    forward_other = measure_other_forward(device, sptr, args, peaks)
+    forward_other = None if args.no_other else measure_other_forward(device, sptr, args, peaks)
 
     # the verify step's tree-mask and paged-cache forms, same bytes and roofline
     verify_ext = None
@@ -819,6 +819,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-other", action="store_true",
+                    help="skip the other prefill configurations (2K, 2K Q x 4, 32K d = 64)")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="--impl reference: seconds of oracle time for the whole run")
     ap.add_argument("--sustained-s", type=float, default=1.5,
