@@ -20,6 +20,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
+FA_ERR_BOUNDS = 6
 FA_VERIFY_MAX_SQ = 16
 FA_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
 FA_HOST_CHUNKS = 16
@@ -52,6 +53,8 @@ SIGNATURES = {
     "fa_selftest_umma_f8": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
     "fa_selftest_wait_timeout": (_I32, [_U64, _P]),
     "fa_testing_stall_next_launch": (_I32, [_I32, _I32, _U64]),
+    "fa_testing_debug_checks": (_I32, []),
+    "fa_selftest_index_check": (_I32, [_I32, _P]),
     "fa_selftest_mufu": (_I32, [_P, _I32, _I32, _P]),
     "fa_selftest_mma_rate": (_I32, [_P, _I32, _I32, _I32, _P]),
 }
@@ -65,12 +68,9 @@ class FAError(RuntimeError):
         super().__init__(f"{what}: {status_string(status)} (status {status})")
 
 
-def load(path: str | None = None):
-    """Load the CUDA library (once). Raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = path or LIB_PATH
+def open_library(path: str):
+    """A handle on a build of the library at `path` (for example the debug build),
+    with every signature set; it does not become the handle the wrappers use."""
     if not os.path.exists(path):
         raise RuntimeError(
             f"the CUDA library {path} is missing; build it with "
@@ -80,8 +80,16 @@ def load(path: str | None = None):
         f = getattr(lib, name)
         f.restype = res
         f.argtypes = args
-    _lib = lib
     return lib
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    _lib = open_library(path or LIB_PATH)
+    return _lib
 
 
 def _ptr(x):
@@ -250,3 +258,11 @@ STALL_VERIFY = 2
 def check(status: int, what: str = "fa call"):
     if status != FA_OK:
         raise FAError(status, what)
+
+
+def fa_testing_debug_checks() -> int:
+    return load().fa_testing_debug_checks()
+
+
+def fa_selftest_index_check(fail, stream=None) -> int:
+    return load().fa_selftest_index_check(int(bool(fail)), _stream(stream))

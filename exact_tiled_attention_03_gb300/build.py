@@ -97,5 +97,15 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     return lib
 
 
+DEBUG_LIB = os.path.join(LIBDIR, "libfa_gb300_debug.so")
+
+
+def build_debug(force: bool = False) -> str:
+    """The debug build: the same sources with FA_DEBUG defined (device-side index
+    checks that record a bit in the status word), as lib/libfa_gb300_debug.so."""
+    return build(force=force, defines=["FA_DEBUG=1"], lib_path=DEBUG_LIB,
+                 build_dir=os.path.join(PKG, "_build_debug"))
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))

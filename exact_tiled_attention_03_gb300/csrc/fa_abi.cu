@@ -390,6 +390,7 @@ const char *fa_status_string(fa_status_t s)
     case FA_ERR_CUDA: return "CUDA runtime or launch error";
     case FA_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
     case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_BOUNDS: return "a debug build's index check failed";
     }
     return "unknown status";
 }
@@ -776,6 +777,8 @@ fa_status_t fa_device_status(void *stream)
         if (cudaMemcpy(di->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
             return FA_ERR_CUDA;
     }
+    if (word & kStatusBounds)
+        return FA_ERR_BOUNDS;
     return (word & kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
@@ -871,6 +874,24 @@ fa_status_t fa_selftest_mma_rate(long long *cycles, int mode, int blocks, int it
         return st;
     return launch_selftest_mma_rate(cycles, mode, blocks, iters, static_cast<cudaStream_t>(stream),
                                     di->status);
+}
+
+int fa_testing_debug_checks(void)
+{
+#ifdef FA_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+fa_status_t fa_selftest_index_check(int fail, void *stream)
+{
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_index_check(fail != 0, static_cast<cudaStream_t>(stream), di->status);
 }
 
 fa_status_t fa_testing_stall_next_launch(int kernel, int skip_index, uint64_t wait_limit_ns)

@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
     if (warp == kKvProducerWarp) {
         if (lane == 0) {
+            fa_check(kv0 < p.Sk && bh < p.BH, p.status);
             mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTile);
             for (int b = 0; b < D / 64; ++b) {
                 tma_load_3d(smem + C::kOffK + b * kBoxBytes, &tm_k, &bars->kv_full, b * 64, kv0, bh);
@@ -395,6 +396,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     tma_load_3d(st + C::kTile + b * kBoxBytes, &tm_do, &bars->full[s], b * 64, q0, bh);
                 }
                 const size_t vrow = static_cast<size_t>(bh) * p.Sq_pad + q0;
+                fa_check(q0 < p.Sq && vrow + kBlock <= static_cast<size_t>(p.BH) * p.Sq_pad, p.status);
                 bulk_load(smem + C::kOffVec + s * 1024, p.lse2 + vrow, 512, &bars->full[s]);
                 bulk_load(smem + C::kOffVec + s * 1024 + 512, p.Dvec + vrow, 512, &bars->full[s]);
             }
@@ -688,6 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stages the zero dQ tile in Q's buffer, which a late load would
         // overwrite.
         if (lane == 0 && n_kv > 0) {
+            fa_check(q0 < p.Sq && bh < p.BH, p.status);
             mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTile);
             for (int b = 0; b < D / 64; ++b) {
                 tma_load_3d(smem + C::kOffQ + b * kBoxBytes, &tm_q, &bars->q_full, b * 64, q0, bh);
@@ -703,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t uk = j / C::kKStages, uv = j / C::kVStages;
                 if (uk > 0 && !mbar_wait(&bars->k_empty[sk], (uk - 1) & 1, abort_flag, p.status))
                     break;
+                fa_check(j * kBlock < p.Sk, p.status);
                 mbar_arrive_expect_tx(&bars->k_full[sk], C::kTile);
                 for (int b = 0; b < D / 64; ++b)
                     tma_load_3d(smem + C::kOffK + sk * C::kTile + b * kBoxBytes, &tm_k,
@@ -830,8 +834,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
         const size_t vrow = static_cast<size_t>(bh) * p.Sq_pad + i;
         // -lse2 and -D of this query (padded rows: -inf, -0)
-        const float2 nl2 = make_float2(p.lse2[vrow], p.lse2[vrow]);
-        const float2 nD = make_float2(p.Dvec[vrow], p.Dvec[vrow]);
+        const bool vrow_ok = fa_check(vrow < static_cast<size_t>(p.BH) * p.Sq_pad, p.status);
+        const float nl = vrow_ok ? p.lse2[vrow] : -INFINITY, nd = vrow_ok ? p.Dvec[vrow] : -0.0f;
+        const float2 nl2 = make_float2(nl, nl);
+        const float2 nD = make_float2(nd, nd);
         const int lim = visible_keys(i, p.Sq, p.Sk, p.causal);
         bool ok = true;
         for (int j = 0; j < n_kv && ok; ++j) {

@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t use = it / kStages;
                 if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status))
                     return false;
+                fa_check(j * kBlockN < p.sc.Sk && bh < p.sc.BH, p.status);
                 mbar_arrive_expect_tx(&bars->kv_full[s], kTileBytes);
                 tma_load_3d_hint(sKV + s * kTileBytes, which == 0 ? &tm_k : &tm_v,
                                  &bars->kv_full[s], 0, j * kBlockN, bh, pol_keep);
@@ -224,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    fa_check(I.q0[t] < p.sc.Sq && I.bh < p.sc.BH, p.status);
                     mbar_arrive_expect_tx(&bars->q_full[t], kTileBytes);
                     tma_load_3d_hint(sQ + t * kTileBytes, &tm_q, &bars->q_full[t], 0, I.q0[t],
                                      p.zero_q ? p.sc.BH : I.bh, pol_stream);
@@ -540,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             named_bar_sync(1 + t, 128);
             if (r == 0) {
+                fa_check(q0 < p.sc.Sq && I.bh < p.sc.BH, p.status);
                 for (int b = 0; b < kD / 64; ++b)
                     tma_store_3d(&tm_o, sOut + b * kOutBoxBytes, b * 64, q0, I.bh);
                 tma_store_commit();
@@ -553,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ? (M - static_cast<float>(kPShift)) * 0.69314718055994531f +
                                             logf(l)
                                       : -INFINITY;
-                p.lse[static_cast<size_t>(I.bh) * p.sc.Sq + i] = lse;
+                if (fa_check(I.bh < p.sc.BH, p.status))
+                    p.lse[static_cast<size_t>(I.bh) * p.sc.Sq + i] = lse;
             }
             release();
         }

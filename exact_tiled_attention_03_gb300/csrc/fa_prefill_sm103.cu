@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++it;
                     return true;
                 }
+                fa_check(j * kBlockN < p.sc.Sk && bh < p.sc.BH, p.status);
                 mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
                 const CUtensorMap *tm = which == 0 ? &tm_k : &tm_v;
                 for (int b = 0; b < C::kBoxes; ++b)
@@ -252,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    fa_check(I.q0[t] < p.sc.Sq && I.bh < p.sc.BH, p.status);
                     mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
                     for (int b = 0; b < C::kBoxes; ++b)
                         tma_load_3d_hint(sQ + t * C::kTileBytes + b * kBoxBytes, &tm_q,
@@ -691,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 named_bar_sync(1 + t, 128);
                 if (r == 0) {
+                    fa_check(q0 < p.sc.Sq && I.bh < p.sc.BH, p.status);
                     tma_store_3d(&tm_o, sOut, b * 64, q0, I.bh);
                     tma_store_commit();
                     // The box may be rewritten (next box, or the next item after
@@ -702,7 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ref is in log2 units: ref * ln 2 is the max in units of the
                 // scaled scores
                 const float lse = (l > 0.0f) ? ref * 0.69314718055994531f + logf(l) : -INFINITY;
-                p.lse[static_cast<size_t>(I.bh) * p.sc.Sq + i] = lse;
+                if (fa_check(I.bh < p.sc.BH, p.status))
+                    p.lse[static_cast<size_t>(I.bh) * p.sc.Sq + i] = lse;
             }
             release();
         }

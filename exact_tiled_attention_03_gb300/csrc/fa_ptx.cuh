@@ -16,6 +16,26 @@ namespace fa {
 
 // Bit set in the device status word when a bounded wait gave up.
 constexpr unsigned int kStatusTimeout = 1u;
+// Bit set by a debug build (FA_DEBUG) when an index check fails.
+constexpr unsigned int kStatusBounds = 2u;
+
+// Index check of the debug build: with FA_DEBUG defined, a false `ok` records
+// kStatusBounds in the device status word and is returned, so that the caller
+// skips the access (plain loads and stores) or only reports it (TMA
+// coordinates, which the hardware bounds itself: skipping a load would strand
+// its barrier). Without FA_DEBUG the check is `true` and compiles away.
+__device__ __forceinline__ bool fa_check(bool ok, unsigned int *status)
+{
+#ifdef FA_DEBUG
+    if (!ok)
+        atomicOr(status, kStatusBounds);
+    return ok;
+#else
+    (void)ok;
+    (void)status;
+    return true;
+#endif
+}
 // Default limit of a bounded wait. A legitimate wait inside these kernels is
 // a few microseconds; two seconds only trips on a broken pipeline.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -421,6 +421,14 @@ __global__ void __launch_bounds__(128, 1)
         tmem_dealloc(tmem, 512);
 }
 
+// One index check, passing or failing as asked (the debug build records a
+// failure in the status word; a release build compiles the check away).
+__global__ void fa_selftest_index_check_kernel(int fail, unsigned int *status)
+{
+    if (threadIdx.x == 0)
+        fa_check(fail == 0, status);
+}
+
 __global__ void fa_selftest_wait_kernel(uint64_t limit_ns, unsigned int *status)
 {
     __shared__ uint64_t bar;
@@ -512,6 +520,12 @@ fa_status_t launch_selftest_mma_rate(long long *cycles, int mode, int blocks, in
         return FA_ERR_CUDA;
     selftest::fa_selftest_mma_rate_kernel<<<blocks, 128, smem, stream>>>(mode, iters, cycles,
                                                                         status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t launch_selftest_index_check(bool fail, cudaStream_t stream, unsigned int *status)
+{
+    selftest::fa_selftest_index_check_kernel<<<1, 32, 0, stream>>>(fail ? 1 : 0, status);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

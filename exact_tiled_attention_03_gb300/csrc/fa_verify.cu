@@ -97,6 +97,8 @@ __device__ __forceinline__ uint32_t draft_mask(const Params &p, int b, int i)
         return all;
     if (p.mode == 1)
         return i >= 31 ? ~0u : ((2u << i) - 1u);
+    if (!fa_check(b < p.BH / p.H, p.status))
+        return 0u;
     return p.tree_mask[static_cast<size_t>(b) * p.Sq + i] & all;
 }
 
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int b = bh / p.H, h = bh % p.H;
     // Keys of this sequence; the draft positions are its last Sq keys.
     int Sk_b = p.Sk;
-    if (kPaged && p.seq_lens) {
+    if (kPaged && p.seq_lens && fa_check(b < p.BH / p.H, p.status)) {
         Sk_b = p.seq_lens[b];
         Sk_b = Sk_b < 0 ? 0 : min(Sk_b, p.max_pages * p.page_size);
     }
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (base != cached) {
                 cached = base;
                 const int idx = base + lane;
-                my_page = idx < n_pages_b
+                my_page = (idx < n_pages_b && fa_check(idx < p.max_pages, p.status))
                               ? p.block_table[static_cast<size_t>(b) * p.max_pages + idx]
                               : p.num_pages;
             }
@@ -248,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint8_t *dst = smem + s * C::kStageBytes;
             const int key = kv_begin + st * kStageKeys;
             if constexpr (!kPaged) {
+                if (lane == 0)
+                    fa_check(key < p.Sk && bh < p.BH, p.status);
                 if (lane == 0)
                     for (int q = 0; q < C::kBoxes; ++q) {
                         tma_load_3d_hint(dst + q * kBoxBytes, &tm_k, &bars->full[s], q * 64, key,
@@ -475,6 +479,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float inv = L > 0.0f ? 1.0f / L : 0.0f;
         const float lse = L > 0.0f ? M * p.scale + logf(L) : -INFINITY;
         const size_t row_g = static_cast<size_t>(bh) * p.Sq + row;
+        if (!fa_check(row_g < static_cast<size_t>(p.BH) * p.Sq && split < p.n_split, p.status))
+            continue;
         if (p.n_split == 1) {
             p.o[row_g * D + col] = __float2bfloat16_rn(acc * inv);
             if (col == 0)

@@ -72,7 +72,8 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, misaligned pointer, no sm_103 device */
     FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
     FA_ERR_TIMEOUT = 4,      /* a kernel's bounded wait ran out (reported by fa_device_status) */
-    FA_ERR_WORKSPACE = 5     /* workspace missing or smaller than fa_workspace_size() */
+    FA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than fa_workspace_size() */
+    FA_ERR_BOUNDS = 6        /* a debug build's index check failed (reported by fa_device_status) */
 } fa_status_t;
 
 /*
@@ -346,9 +347,11 @@ const char *fa_status_string(fa_status_t status);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status
- * word on the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel gave up
- * on a bounded wait since the last call (its outputs are then undefined).
- * Returns FA_ERR_CUDA if the synchronisation itself fails.
+ * word on the current device: FA_OK; FA_ERR_BOUNDS if, in a library built
+ * with FA_DEBUG (device-side index checks; see fa_testing.h), a check failed
+ * since the last call (the access was skipped); else FA_ERR_TIMEOUT if a
+ * kernel gave up on a bounded wait since the last call (its outputs are then
+ * undefined). Returns FA_ERR_CUDA if the synchronisation itself fails.
  */
 fa_status_t fa_device_status(void *stream);
 

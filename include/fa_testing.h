@@ -101,6 +101,23 @@ fa_status_t fa_selftest_mma_rate(long long *cycles, int mode, int blocks, int it
 fa_status_t fa_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 
 /*
+ * Device-side index checks. A library compiled with FA_DEBUG defined (the
+ * debug build, lib/libfa_gb300_debug.so, made by build.build_debug()) checks
+ * the index arithmetic of its kernels before each plain global load or store
+ * (skipping the access if the check fails) and the coordinates of each TMA
+ * copy (reported only: the hardware bounds those itself). A failed check sets
+ * a bit in the device status word, which fa_device_status() reports as
+ * FA_ERR_BOUNDS. Nothing asserts or traps. Release builds compile the checks
+ * away.
+ * fa_testing_debug_checks: 1 in a debug build, 0 otherwise.
+ * fa_selftest_index_check: launches one check that passes (fail == 0) or
+ * fails (fail != 0); in a debug build a failing one makes the next
+ * fa_device_status() return FA_ERR_BOUNDS.
+ */
+int fa_testing_debug_checks(void);
+fa_status_t fa_selftest_index_check(int fail, void *stream);
+
+/*
  * Makes the next launch of one production kernel stall on purpose, so that
  * its bounded waits run out and its abort path runs (set the abort flag,
  * record FA_ERR_TIMEOUT in the device status word, drain the copies and MMAs
