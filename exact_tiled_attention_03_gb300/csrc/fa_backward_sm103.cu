@@ -405,7 +405,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status);
         }
     } else if (warp == kKvMmaWarp) {
-        if (lane == 0 && n_q > 0) {
+        if (n_q > 0) {
+            // The whole warp runs the issue loop (counters and descriptors stay
+            // warp-uniform): it polls each barrier together, and one elected
+            // lane issues each MMA and commit.
+            auto wwait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+            };
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlock, kBlock, false, false);
             constexpr uint32_t idesc_g = idesc_bf16_f32(kBlock, D, false, true);
             const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
@@ -420,10 +426,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + (dp ? C::kColDP : C::kColS), a0 + koff, b0 + koff,
+                    umma_bf16_ss_elect(tmem + (dp ? C::kColDP : C::kColS), a0 + koff, b0 + koff,
                                  dp ? idesc_s : idesc_s | p.idesc_s_neg, kk > 0);
                 }
-                umma_commit(dp ? &bars->dp_full : &bars->s_full);
+                umma_commit_elect(dp ? &bars->dp_full : &bars->s_full);
             };
             // dV += P^T dO (A = P^T from the S columns) or dK += dS^T Q (A =
             // dS^T from the dP columns). A is bf16 pairs, each 32-query group
@@ -436,13 +442,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 const uint32_t a0 = tmem + (dk ? C::kColDP : C::kColS);
 #pragma unroll
                 for (int kk = 0; kk < kBlock / 16; ++kk)
-                    umma_bf16_ts(tmem + (dk ? C::kColDK : C::kColDV),
+                    umma_bf16_ts_elect(tmem + (dk ? C::kColDK : C::kColDV),
                                  a0 + (kk / 2) * kChunk + (kk % 2) * 8,
                                  b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (n > 0 || kk > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.status) &&
-                      mbar_wait(&bars->full[0], 0, abort_flag, p.status);
+            bool ok = wwait(&bars->kv_full, 0) &&
+                      wwait(&bars->full[0], 0);
             if (ok) {
                 tc_fence_after_sync();
                 issue_scores(0, false);
@@ -455,32 +461,33 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             // after its reader; the math warps read S^T (dP^T) before they
             // signal P^T (dS^T).
             for (int n = 0; n < n_q && ok; ++n) {
-                ok = mbar_wait(&bars->p_full, n & 1, abort_flag, p.status);
+                ok = wwait(&bars->p_full, n & 1);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
                 issue_grad(n, false);
                 const bool next = n + 1 < n_q;
                 if (next) {
-                    ok = mbar_wait(&bars->full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1,
-                                   abort_flag, p.status);
+                    ok = wwait(&bars->full[(n + 1) % C::kStages], ((n + 1) / C::kStages) & 1);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
                     issue_scores(n + 1, false);
                 }
-                ok = mbar_wait(&bars->ds_full, n & 1, abort_flag, p.status);
+                ok = wwait(&bars->ds_full, n & 1);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
                 issue_grad(n, true);
-                umma_commit(&bars->empty[n % C::kStages]);
+                umma_commit_elect(&bars->empty[n % C::kStages]);
                 if (next)
                     issue_scores(n + 1, true);
             }
-            umma_commit(&bars->o_done);
-            umma_commit(&bars->drain);
-            mbar_wait_drain(&bars->drain, 0, p.status);
+            umma_commit_elect(&bars->o_done);
+            umma_commit_elect(&bars->drain);
+            if (lane == 0)
+                mbar_wait_drain(&bars->drain, 0, p.status);
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ math warps
@@ -730,7 +737,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_drain(&bars->v_full[k % C::kVStages], (k / C::kVStages) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0 && n_kv > 0) {
+        if (n_kv > 0) {
+            // The whole warp runs the issue loop (counters and descriptors stay
+            // warp-uniform): it polls each barrier together, and one elected
+            // lane issues each MMA and commit.
+            auto wwait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+            };
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlock, kBlock, false, false);
             constexpr uint32_t idesc_g = idesc_bf16_f32(kBlock, D, false, true);
             const uint64_t aq0 = smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
@@ -747,14 +760,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + col, a0 + koff, b0 + koff,
+                    umma_bf16_ss_elect(tmem + col, a0 + koff, b0 + koff,
                                  dp ? idesc_s : idesc_s | p.idesc_s_neg, kk > 0);
                 }
                 if (dp) {
-                    umma_commit(&bars->dp_full);
-                    umma_commit(&bars->v_empty[j % C::kVStages]);
+                    umma_commit_elect(&bars->dp_full);
+                    umma_commit_elect(&bars->v_empty[j % C::kVStages]);
                 } else {
-                    umma_commit(&bars->s_full[j & 1]);
+                    umma_commit_elect(&bars->s_full[j & 1]);
                 }
             };
             // dQ += dS K_j: A = dS (bf16 pairs: keys 0-63 in the dP region's
@@ -764,18 +777,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t bkm = smem_desc_sw128(sk, kBoxBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBlock / 16; ++kk)
-                    umma_bf16_ts(tmem + C::kColDQ, tmem + C::kColDP + (kk / 4) * kHalf + (kk % 4) * 8,
+                    umma_bf16_ts_elect(tmem + C::kColDQ, tmem + C::kColDP + (kk / 4) * kHalf + (kk % 4) * 8,
                                  bkm + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_g,
                                  (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->k_empty[j % C::kKStages]);
+                umma_commit_elect(&bars->k_empty[j % C::kKStages]);
             };
             auto wait_k = [&](int j) {
-                return mbar_wait(&bars->k_full[j % C::kKStages], (j / C::kKStages) & 1, abort_flag,
-                                 p.status);
+                return wwait(&bars->k_full[j % C::kKStages], (j / C::kKStages) & 1);
             };
             auto wait_v = [&](int j) {
-                return mbar_wait(&bars->v_full[j % C::kVStages], (j / C::kVStages) & 1, abort_flag,
-                                 p.status);
+                return wwait(&bars->v_full[j % C::kVStages], (j / C::kVStages) & 1);
             };
             // Issue order: S(0) dP(0) S(1) | dQ(0) dP(1) S(2) | dQ(1) dP(2) S(3) | ...
             // dS(j) is rebuilt while dP(j)'s successors S(j+1) (and the
@@ -783,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // read dS(j) from them, and S(j+2) reuses S(j)'s buffer; MMAs
             // from one thread run in issue order, and the math warps read
             // S(j) and dP(j) before they signal dS(j).
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status) && wait_k(0);
+            bool ok = wwait(&bars->q_full, 0) && wait_k(0);
             if (ok) {
                 tc_fence_after_sync();
                 issue_scores(0, false);
@@ -801,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int j = 0; j < n_kv && ok; ++j) {
-                ok = mbar_wait(&bars->ds_full, j & 1, abort_flag, p.status);
+                ok = wwait(&bars->ds_full, j & 1);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
@@ -821,9 +832,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_scores(j + 2, false);
                 }
             }
-            umma_commit(&bars->o_done);
-            umma_commit(&bars->drain);
-            mbar_wait_drain(&bars->drain, 0, p.status);
+            umma_commit_elect(&bars->o_done);
+            umma_commit_elect(&bars->drain);
+            if (lane == 0)
+                mbar_wait_drain(&bars->drain, 0, p.status);
+            __syncwarp();
         }
     } else {
         const int quarter = warp & 3, half = warp >> 2;

@@ -20,7 +20,8 @@
 //     K_j, V_j through a ring of shared-memory stages with TMA (128-byte
 //     swizzle), one mbarrier pair per stage. The next item's first loads and
 //     S MMAs run while the softmax warps finish the current item;
-//   * warp 9 (one elected thread) issues tcgen05.mma: S_t = Q_t K_j^T into
+//   * warp 9 issues tcgen05.mma (the whole warp runs the issue loop, one
+//     lane elected per MMA): S_t = Q_t K_j^T into
 //     tensor memory (TMEM), and O_t += P_t V_j with P_t read from TMEM and V
 //     read MN-major straight from its row-major tile; completion is signalled
 //     with tcgen05.commit. Issue order per key tile j: PV_0(j), S_0(j+1),
@@ -280,7 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // that held P_t(j), and the next item's PV_t(0) overwrites O_t; the
         // tensor pipe executes one thread's MMAs in order, and the softmax
         // warps have read O_t (epilogue) before they publish the next P_t.
-        if (lane == 0) {
+        // The whole warp runs the loop (its counters and descriptors stay
+        // warp-uniform); the warp polls each barrier together, and one elected
+        // lane issues each MMA and commit.
+        {
             const uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false) | p.idesc_qk_neg;
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
             const uint32_t colS[kTiles] = {C::kColS0, C::kColS1};
@@ -298,34 +302,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t koff = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_bf16_ss(tmem + colS[t], a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                    umma_bf16_ss_elect(tmem + colS[t], a0 + koff, b0 + koff, idesc_qk,
+                                       kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int slot, int j) {
                 const uint64_t b0 = dv0 + kTileStep * slot;
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    umma_bf16_ts(tmem + colO[t], tmem + colS[t] + kk * 8,
-                                 b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts_elect(tmem + colO[t], tmem + colS[t] + kk * 8,
+                                       b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+            };
+            // A bounded wait polled by the whole warp together (each poll is one
+            // warp instruction, and the warp sleeps in it), made warp-uniform.
+            auto wwait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu,
+                                  mbar_wait(bar, parity, abort_flag, p.status, p.wait_ns));
             };
             auto ring_wait = [&](int idx) {
-                return mbar_wait(&bars->kv_full[idx % C::kStages], (idx / C::kStages) & 1,
-                                 abort_flag, p.status, p.wait_ns);
+                return wwait(&bars->kv_full[idx % C::kStages], (idx / C::kStages) & 1);
             };
             int it = 0;
             uint32_t q_waits[kTiles] = {0, 0}, p_waits[kTiles] = {0, 0};
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 const int slot = n % kQueue;
-                if (!mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status, p.wait_ns))
+                if (!wwait(&bars->item_full[slot], (n / kQueue) & 1))
                     break;
-                const int w = bars->items[slot];
+                const int w = __shfl_sync(0xffffffffu, lane == 0 ? bars->items[slot] : 0, 0);
                 if (w < 0)
                     break;
                 const Item I = sched::decode_item(w, p.sc);
                 if (I.n_kv_max == 0) {
-                    mbar_arrive(&bars->item_empty[slot]);
+                    if (lane == 0)
+                        mbar_arrive(&bars->item_empty[slot]);
                     continue;
                 }
                 // S_t(0) as soon as Q_t is in: tile 0's Q buffer frees a key
@@ -334,16 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < kTiles && ok; ++t) {
                     if (I.n_kv[t] == 0)
                         continue;
-                    ok = mbar_wait(&bars->q_full[t], (q_waits[t]++) & 1, abort_flag, p.status, p.wait_ns);
+                    ok = wwait(&bars->q_full[t], (q_waits[t]++) & 1);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
                     issue_s(t, it % C::kStages);
-                    umma_commit(&bars->s_full[t]);
+                    umma_commit_elect(&bars->s_full[t]);
                 }
                 if (!ok)
                     break;
-                umma_commit(&bars->kv_empty[it % C::kStages]);
+                umma_commit_elect(&bars->kv_empty[it % C::kStages]);
                 for (int j = 0; j < I.n_kv_max && ok; ++j) {
                     const int iv = it + 2 * j + 1, ik = it + 2 * j + 2;
                     ok = ring_wait(iv);  // V_j
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < kTiles && ok; ++t) {
                         if (j >= I.n_kv[t])
                             continue;
-                        ok = mbar_wait(&bars->p_full[t], (p_waits[t]++) & 1, abort_flag, p.status, p.wait_ns);
+                        ok = wwait(&bars->p_full[t], (p_waits[t]++) & 1);
                         if (!ok)
                             break;
                         tc_fence_after_sync();
@@ -368,23 +379,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 k_ready = true;
                             }
                             issue_s(t, ik % C::kStages);
-                            umma_commit(&bars->s_full[t]);
+                            umma_commit_elect(&bars->s_full[t]);
                         } else {
-                            umma_commit(&bars->o_done[t]);  // this tile's last PV of the item
+                            umma_commit_elect(&bars->o_done[t]);  // this tile's last PV of the item
                         }
                     }
                     if (!ok)
                         break;
-                    umma_commit(&bars->kv_empty[iv % C::kStages]);
+                    umma_commit_elect(&bars->kv_empty[iv % C::kStages]);
                     if (k_ready)
-                        umma_commit(&bars->kv_empty[ik % C::kStages]);
+                        umma_commit_elect(&bars->kv_empty[ik % C::kStages]);
                 }
                 it += 2 * I.n_kv_max;
-                mbar_arrive(&bars->item_empty[slot]);  // every MMA of the item is issued
+                if (lane == 0)
+                    mbar_arrive(&bars->item_empty[slot]);  // every MMA of the item is issued
             }
-            // Drain: all MMAs issued by this thread complete before TMEM is freed.
-            umma_commit(&bars->drain);
-            mbar_wait_drain(&bars->drain, 0, p.status, p.wait_ns);
+            // Drain: all MMAs issued by the elected lane complete before TMEM is freed.
+            umma_commit_elect(&bars->drain);
+            if (lane == 0)
+                mbar_wait_drain(&bars->drain, 0, p.status, p.wait_ns);
+            __syncwarp();
         }
     } else if (warp < kSoftmaxWarps) {
         // ------------------------------------------------------------ softmax warpgroups
