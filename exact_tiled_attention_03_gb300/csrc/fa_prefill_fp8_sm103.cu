@@ -502,6 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 release();
                 continue;
             }
+            // The previous item's stores may still be reading the staging
+            // buffer: their issuer waits here, before the barrier below, so the
+            // buffer is rewritten only after those reads (the wait is not taken
+            // at the end of that epilogue, where it sat on the tile's critical path).
+            if (r == 0)
+                tma_store_wait_read_all();
             bool got = ok;
             if (got && n_kv > 0) {
                 got = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (o_waits++) & 1,
@@ -546,9 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int b = 0; b < kD / 64; ++b)
                     tma_store_3d(&tm_o, sOut + b * kOutBoxBytes, b * 64, q0, I.bh);
                 tma_store_commit();
-                // The buffer is rewritten only after the tile's next barrier;
-                // the writes finish on their own.
-                tma_store_wait_read_all();
+                // The reads of the buffer are waited for at the next epilogue;
+                // the writes to global memory finish on their own.
             }
             if (i < p.sc.Sq) {
                 // lse = ln 2 * (M - kPShift + log2 l), in units of the scaled scores
