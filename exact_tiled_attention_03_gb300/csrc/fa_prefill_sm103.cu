@@ -68,10 +68,10 @@ constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (1
 // Lazy rescale threshold, in log2 units of the exponent (factor 256).
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kRescaleFactor = 256.0f;  // 2^kRescaleLog2
-// Largest move of the reference made by shifting the p already computed
-// (2^kShiftLog2 stays far inside fp32 and bf16 range); larger jumps recompute.
-constexpr float kShiftLog2 = 100.0f;
-constexpr float kShiftLimit = 1.2676506e30f;  // 2^kShiftLog2
+// d = 128: largest row sum settled by shifting the p already computed (below it
+// no p can have overflowed, and 2^100 stays far inside fp32 and bf16 range); a
+// larger sum recomputes against the exact max.
+constexpr float kShiftLimit = 0x1p100f;
 
 template <int D>
 struct Cfg {
@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // reference, p is computed against it. Every p is >= 0, so a row
                     // sum of at most 2^kRescaleLog2 shows that no p exceeds
                     // 2^kRescaleLog2 and the reference stays. A larger sum (up to
-                    // 2^kShiftLimit, so that no p can have overflowed) is settled
+                    // kShiftLimit, so that no p can have overflowed) is settled
                     // from the packed p: their max, and a shift by its exponent when
                     // it exceeds 2^kRescaleLog2. Only a larger sum, or a row's first
                     // tile, runs the max pass and then the exponentials against the
