@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             // Issue order: ... dP(n) | dV(n) S(n+1) | dK(n) dP(n+1) | dV(n+1) ...
             // Each rebuild (P^T after S^T lands, dS^T after dP^T lands) has
             // two 128-wide MMAs ahead of the one that consumes it. MMAs from
-            // one thread run in issue order, which orders each TMEM reuse
+            // one lane run in issue order, which orders each TMEM reuse
             // after its reader; the math warps read S^T (dP^T) before they
             // signal P^T (dS^T).
             for (int n = 0; n < n_q && ok; ++n) {
@@ -792,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dS(j) is rebuilt while dP(j)'s successors S(j+1) (and the
             // previous dQ) execute. dP(j+1) reuses dP's columns after dQ(j)
             // read dS(j) from them, and S(j+2) reuses S(j)'s buffer; MMAs
-            // from one thread run in issue order, and the math warps read
+            // from one lane run in issue order, and the math warps read
             // S(j) and dP(j) before they signal dS(j).
             bool ok = wwait(&bars->q_full, 0) && wait_k(0);
             if (ok) {

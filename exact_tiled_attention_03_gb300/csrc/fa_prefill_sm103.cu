@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kQueue; ++s) {
             mbar_init(&bars->item_full[s], 1);
-            mbar_init(&bars->item_empty[s], 1 + kSoftmaxWarps);  // MMA thread + softmax warps
+            mbar_init(&bars->item_empty[s], 1 + kSoftmaxWarps);  // MMA warp + softmax warps
         }
         mbar_init(&bars->drain, 1);
         for (int s = 0; s < C::kStages; ++s) {
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           p.wait_ns))
                     return false;
                 if (it == p.stall_load && blockIdx.x == 0) {
-                    // Test only: this load is never issued, so the MMA thread's
+                    // Test only: this load is never issued, so the MMA warp's
                     // bounded wait for it runs out and the CTA takes its abort path.
                     ++it;
                     return true;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the same order. Issue order: S_0(0), S_1(0), then per j: PV_0(j),
         // S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites the TMEM columns
         // that held P_t(j), and the next item's PV_t(0) overwrites O_t; the
-        // tensor pipe executes one thread's MMAs in order, and the softmax
+        // tensor pipe executes one lane's MMAs in order, and the softmax
         // warps have read O_t (epilogue) before they publish the next P_t.
         // The whole warp runs the loop (its counters and descriptors stay
         // warp-uniform); the warp polls each barrier together, and one elected
