@@ -55,6 +55,7 @@ SIGNATURES = {
     "fa_testing_stall_next_launch": (_I32, [_I32, _I32, _U64]),
     "fa_testing_debug_checks": (_I32, []),
     "fa_selftest_index_check": (_I32, [_I32, _P]),
+    "fa_selftest_elect": (_I32, [_P, _I32, _P]),
     "fa_selftest_mufu": (_I32, [_P, _I32, _I32, _P]),
     "fa_selftest_mma_rate": (_I32, [_P, _I32, _I32, _I32, _P]),
 }
@@ -266,3 +267,7 @@ def fa_testing_debug_checks() -> int:
 
 def fa_selftest_index_check(fail, stream=None) -> int:
     return load().fa_selftest_index_check(int(bool(fail)), _stream(stream))
+
+
+def fa_selftest_elect(lanes, trials, stream=None) -> int:
+    return load().fa_selftest_elect(_ptr(lanes), int(trials), _stream(stream))

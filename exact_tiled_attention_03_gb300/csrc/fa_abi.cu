@@ -894,6 +894,19 @@ fa_status_t fa_selftest_index_check(int fail, void *stream)
     return launch_selftest_index_check(fail != 0, static_cast<cudaStream_t>(stream), di->status);
 }
 
+fa_status_t fa_selftest_elect(int *lanes, int trials, void *stream)
+{
+    if (!lanes || trials <= 0 || trials > (1 << 20))
+        return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(lanes) % alignof(int) != 0)
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *di = nullptr;
+    fa_status_t st = device_ok(&di);
+    if (st != FA_OK)
+        return st;
+    return launch_selftest_elect(lanes, trials, static_cast<cudaStream_t>(stream));
+}
+
 fa_status_t fa_testing_stall_next_launch(int kernel, int skip_index, uint64_t wait_limit_ns)
 {
     if ((kernel != kStallPrefill && kernel != kStallVerify) || skip_index < 0 ||

@@ -90,6 +90,7 @@ fa_status_t launch_selftest_umma_ts(const void *a, const void *b, float *c, int 
                                     int b_mn_major, cudaStream_t stream, unsigned int *status);
 fa_status_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t stream, unsigned int *status);
 fa_status_t launch_selftest_index_check(bool fail, cudaStream_t stream, unsigned int *status);
+fa_status_t launch_selftest_elect(int *lanes, int trials, cudaStream_t stream);
 fa_status_t launch_selftest_mufu(float *out, int blocks, int iters, cudaStream_t stream);
 fa_status_t launch_selftest_mma_rate(long long *cycles, int mode, int blocks, int iters,
                                      cudaStream_t stream, unsigned int *status);

@@ -429,6 +429,30 @@ __global__ void fa_selftest_index_check_kernel(int fail, unsigned int *status)
         fa_check(fail == 0, status);
 }
 
+// The lane elect.sync picks in a converged warp, `trials` times per warp (4
+// warps), into lanes[warp * trials + i]. Before each election the lanes run
+// loops of lane-dependent length and reconverge, so that the election does
+// not follow a uniform history. The MMA issue loops rely on every election
+// of the warp picking the same lane: a commit tracks only the MMAs its own
+// thread issued.
+__global__ void fa_selftest_elect_kernel(int *lanes, int trials)
+{
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    volatile int sink = 0;
+    for (int i = 0; i < trials; ++i) {
+        for (int k = 0; k < ((lane * 7 + i) % 5); ++k)
+            sink = sink + k;
+        __syncwarp();
+        uint32_t elected;
+        asm volatile(
+            "{\n\t.reg .pred e;\n\t"
+            "elect.sync %0|e, 0xffffffff;\n\t}"
+            : "=r"(elected));
+        if (lane == 0)
+            lanes[warp * trials + i] = static_cast<int>(elected);
+    }
+}
+
 __global__ void fa_selftest_wait_kernel(uint64_t limit_ns, unsigned int *status)
 {
     __shared__ uint64_t bar;
@@ -526,6 +550,12 @@ fa_status_t launch_selftest_mma_rate(long long *cycles, int mode, int blocks, in
 fa_status_t launch_selftest_index_check(bool fail, cudaStream_t stream, unsigned int *status)
 {
     selftest::fa_selftest_index_check_kernel<<<1, 32, 0, stream>>>(fail ? 1 : 0, status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t launch_selftest_elect(int *lanes, int trials, cudaStream_t stream)
+{
+    selftest::fa_selftest_elect_kernel<<<1, 128, 0, stream>>>(lanes, trials);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -118,6 +118,21 @@ int fa_testing_debug_checks(void);
 fa_status_t fa_selftest_index_check(int fail, void *stream);
 
 /*
+ * The lane that elect.sync picks in a converged warp. The MMA-issuing warps
+ * of the prefill and backward kernels run their issue loops as a whole warp
+ * and let elect.sync pick the lane that issues each tcgen05.mma and each
+ * tcgen05.commit; a commit tracks only its own thread's MMAs, so every
+ * election must pick the same lane. Launches one CTA of 4 warps; each warp
+ * runs `trials` elections (after lane-dependent work and a reconvergence)
+ * and writes the elected lane id of election i to lanes[warp * trials + i].
+ *   lanes  : device int[4 * trials], caller-owned, written by the kernel
+ *   trials : 1 .. 2^20
+ * FA_ERR_INVALID_ARG for a null pointer or a count out of range;
+ * asynchronous on `stream`.
+ */
+fa_status_t fa_selftest_elect(int *lanes, int trials, void *stream);
+
+/*
  * Makes the next launch of one production kernel stall on purpose, so that
  * its bounded waits run out and its abort path runs (set the abort flag,
  * record FA_ERR_TIMEOUT in the device status word, drain the copies and MMAs

@@ -180,6 +180,8 @@ def test_testing_entry_points_validate_first(capi):
     assert capi.fa_selftest_umma(None, ALIGNED, ALIGNED, 128, 128, 0, 0) == capi.FA_ERR_INVALID_ARG
     assert capi.fa_selftest_umma(ALIGNED, ALIGNED, ALIGNED, 96, 128, 0, 0) == capi.FA_ERR_INVALID_ARG
     assert capi.fa_selftest_wait_timeout(0, 0) == capi.FA_ERR_INVALID_ARG
+    assert capi.fa_selftest_elect(None, 4, 0) == capi.FA_ERR_INVALID_ARG
+    assert capi.fa_selftest_elect(ALIGNED, 0, 0) == capi.FA_ERR_INVALID_ARG
     assert capi.fa_reference_forward_simt(None, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 1, 1, 4, 4, 8,
                                           0, 0.5, 0) == capi.FA_ERR_INVALID_ARG
 

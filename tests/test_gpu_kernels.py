@@ -71,6 +71,17 @@ def test_mufu_microbenchmark_runs():
     assert ((v / 8 + 0.59).abs() < 0.02).all()
 
 
+def test_elect_sync_picks_the_same_lane_every_time():
+    """The warp-wide MMA issue loops let elect.sync pick the issuing lane for
+    each MMA and each commit separately; a commit tracks only its own thread's
+    MMAs, so every election of a converged warp must pick the same lane."""
+    trials = 256
+    lanes = torch.full((4 * trials,), -1, dtype=torch.int32, device="cuda")
+    _capi.check(_capi.fa_selftest_elect(lanes, trials), "elect")
+    torch.cuda.synchronize()
+    assert (lanes.cpu() == 0).all()
+
+
 def test_mma_rate_of_the_operand_forms():
     """The gradient kernels issue only 128-wide MMAs because two 64-wide halves
     take longer than one 128-wide MMA of the same work (measured 45-54 against 64
