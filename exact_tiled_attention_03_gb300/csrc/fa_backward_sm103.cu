@@ -375,34 +375,50 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     int *abort_flag = &bars->abort_flag;
 
     if (warp == kKvProducerWarp) {
-        if (lane == 0) {
-            fa_check(kv0 < p.Sk && bh < p.BH, p.status);
-            mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTile);
-            for (int b = 0; b < D / 64; ++b) {
-                tma_load_3d(smem + C::kOffK + b * kBoxBytes, &tm_k, &bars->kv_full, b * 64, kv0, bh);
-                tma_load_3d(smem + C::kOffV + b * kBoxBytes, &tm_v, &bars->kv_full, b * 64, kv0, bh);
+        {
+            // The whole warp runs the loop and polls each barrier together;
+            // lane 0 alone issues the copies.
+            auto wwait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+            };
+            if (lane == 0) {
+                fa_check(kv0 < p.Sk && bh < p.BH, p.status);
+                mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTile);
+                for (int b = 0; b < D / 64; ++b) {
+                    tma_load_3d(smem + C::kOffK + b * kBoxBytes, &tm_k, &bars->kv_full, b * 64, kv0, bh);
+                    tma_load_3d(smem + C::kOffV + b * kBoxBytes, &tm_v, &bars->kv_full, b * 64, kv0, bh);
+                }
             }
+            __syncwarp();
             int n = 0;
             for (; n < n_q; ++n) {
                 const int s = n % C::kStages;
                 const uint32_t use = n / C::kStages;
-                if (use > 0 && !mbar_wait(&bars->empty[s], (use - 1) & 1, abort_flag, p.status))
+                if (use > 0 && !wwait(&bars->empty[s], (use - 1) & 1))
                     break;
-                const int q0 = (qt0 + n) * kBlock;
-                uint8_t *st = smem + C::kOffRing + s * C::kStageBytes;
-                mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes + 1024);
-                for (int b = 0; b < D / 64; ++b) {
-                    tma_load_3d(st + b * kBoxBytes, &tm_q, &bars->full[s], b * 64, q0, bh);
-                    tma_load_3d(st + C::kTile + b * kBoxBytes, &tm_do, &bars->full[s], b * 64, q0, bh);
+                if (lane == 0) {
+                    const int q0 = (qt0 + n) * kBlock;
+                    uint8_t *st = smem + C::kOffRing + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes + 1024);
+                    for (int b = 0; b < D / 64; ++b) {
+                        tma_load_3d(st + b * kBoxBytes, &tm_q, &bars->full[s], b * 64, q0, bh);
+                        tma_load_3d(st + C::kTile + b * kBoxBytes, &tm_do, &bars->full[s], b * 64, q0,
+                                    bh);
+                    }
+                    const size_t vrow = static_cast<size_t>(bh) * p.Sq_pad + q0;
+                    fa_check(q0 < p.Sq && vrow + kBlock <= static_cast<size_t>(p.BH) * p.Sq_pad,
+                             p.status);
+                    bulk_load(smem + C::kOffVec + s * 1024, p.lse2 + vrow, 512, &bars->full[s]);
+                    bulk_load(smem + C::kOffVec + s * 1024 + 512, p.Dvec + vrow, 512, &bars->full[s]);
                 }
-                const size_t vrow = static_cast<size_t>(bh) * p.Sq_pad + q0;
-                fa_check(q0 < p.Sq && vrow + kBlock <= static_cast<size_t>(p.BH) * p.Sq_pad, p.status);
-                bulk_load(smem + C::kOffVec + s * 1024, p.lse2 + vrow, 512, &bars->full[s]);
-                bulk_load(smem + C::kOffVec + s * 1024 + 512, p.Dvec + vrow, 512, &bars->full[s]);
+                __syncwarp();
             }
-            mbar_wait_drain(&bars->kv_full, 0, p.status);
-            for (int k = max(0, n - C::kStages); k < n; ++k)
-                mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status);
+            if (lane == 0) {
+                mbar_wait_drain(&bars->kv_full, 0, p.status);
+                for (int k = max(0, n - C::kStages); k < n; ++k)
+                    mbar_wait_drain(&bars->full[k % C::kStages], (k / C::kStages) & 1, p.status);
+            }
+            __syncwarp();
         }
     } else if (warp == kKvMmaWarp) {
         if (n_q > 0) {
@@ -696,13 +712,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // A query tile that sees no key tile loads nothing: its epilogue
         // stages the zero dQ tile in Q's buffer, which a late load would
         // overwrite.
-        if (lane == 0 && n_kv > 0) {
-            fa_check(q0 < p.Sq && bh < p.BH, p.status);
-            mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTile);
-            for (int b = 0; b < D / 64; ++b) {
-                tma_load_3d(smem + C::kOffQ + b * kBoxBytes, &tm_q, &bars->q_full, b * 64, q0, bh);
-                tma_load_3d(smem + C::kOffDO + b * kBoxBytes, &tm_do, &bars->q_full, b * 64, q0, bh);
+        if (n_kv > 0) {
+            // The whole warp runs the loop and polls each barrier together;
+            // lane 0 alone issues the copies.
+            auto wwait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+            };
+            if (lane == 0) {
+                fa_check(q0 < p.Sq && bh < p.BH, p.status);
+                mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTile);
+                for (int b = 0; b < D / 64; ++b) {
+                    tma_load_3d(smem + C::kOffQ + b * kBoxBytes, &tm_q, &bars->q_full, b * 64, q0, bh);
+                    tma_load_3d(smem + C::kOffDO + b * kBoxBytes, &tm_do, &bars->q_full, b * 64, q0, bh);
+                }
             }
+            __syncwarp();
             // K_j then V_j: V_j's slot frees (dP(j - kVStages) done) before
             // K_{j+1}'s (dQ(j + 1 - kKStages) done), so neither wait holds
             // up a copy that could already start.
@@ -711,30 +735,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (; j < n_kv && ok; ++j) {
                 const int sk = j % C::kKStages, sv = j % C::kVStages;
                 const uint32_t uk = j / C::kKStages, uv = j / C::kVStages;
-                if (uk > 0 && !mbar_wait(&bars->k_empty[sk], (uk - 1) & 1, abort_flag, p.status))
+                if (uk > 0 && !wwait(&bars->k_empty[sk], (uk - 1) & 1))
                     break;
-                fa_check(j * kBlock < p.Sk, p.status);
-                mbar_arrive_expect_tx(&bars->k_full[sk], C::kTile);
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(smem + C::kOffK + sk * C::kTile + b * kBoxBytes, &tm_k,
-                                &bars->k_full[sk], b * 64, j * kBlock, bh);
-                if (uv > 0 && !mbar_wait(&bars->v_empty[sv], (uv - 1) & 1, abort_flag, p.status)) {
+                if (lane == 0) {
+                    fa_check(j * kBlock < p.Sk, p.status);
+                    mbar_arrive_expect_tx(&bars->k_full[sk], C::kTile);
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(smem + C::kOffK + sk * C::kTile + b * kBoxBytes, &tm_k,
+                                    &bars->k_full[sk], b * 64, j * kBlock, bh);
+                }
+                __syncwarp();
+                if (uv > 0 && !wwait(&bars->v_empty[sv], (uv - 1) & 1)) {
                     ok = false;  // K_j is in flight: drain it below
                     ++j;
                     break;
                 }
-                mbar_arrive_expect_tx(&bars->v_full[sv], C::kTile);
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(smem + C::kOffV + sv * C::kTile + b * kBoxBytes, &tm_v,
-                                &bars->v_full[sv], b * 64, j * kBlock, bh);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars->v_full[sv], C::kTile);
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(smem + C::kOffV + sv * C::kTile + b * kBoxBytes, &tm_v,
+                                    &bars->v_full[sv], b * 64, j * kBlock, bh);
+                }
+                __syncwarp();
             }
             // Drain the copies in flight (at most the last ring's worth of each).
-            mbar_wait_drain(&bars->q_full, 0, p.status);
-            const int nk = j, nv = ok ? j : j - 1;
-            for (int k = max(0, nk - C::kKStages); k < nk; ++k)
-                mbar_wait_drain(&bars->k_full[k % C::kKStages], (k / C::kKStages) & 1, p.status);
-            for (int k = max(0, nv - C::kVStages); k < nv; ++k)
-                mbar_wait_drain(&bars->v_full[k % C::kVStages], (k / C::kVStages) & 1, p.status);
+            if (lane == 0) {
+                mbar_wait_drain(&bars->q_full, 0, p.status);
+                const int nk = j, nv = ok ? j : j - 1;
+                for (int k = max(0, nk - C::kKStages); k < nk; ++k)
+                    mbar_wait_drain(&bars->k_full[k % C::kKStages], (k / C::kKStages) & 1, p.status);
+                for (int k = max(0, nv - C::kVStages); k < nv; ++k)
+                    mbar_wait_drain(&bars->v_full[k % C::kVStages], (k / C::kVStages) & 1, p.status);
+            }
+            __syncwarp();
         }
     } else if (warp == kMmaWarp) {
         if (n_kv > 0) {

@@ -180,7 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Takes work items from the launch's counter, publishes each to the
         // other roles through the item queue, then loads its Q tiles and its
         // K_j, V_j through the ring, as the bf16 kernel does.
-        if (lane == 0) {
+        // The whole warp runs the loop and polls each barrier together; lane 0
+        // alone takes items and issues the copies and arrivals.
+        {
             const uint64_t pol_stream = l2_policy_evict_first();  // Q: read once
             const uint64_t pol_keep = l2_policy_evict_last();     // K/V: re-read by other q-blocks
             int it = 0;                         // ring index, continuous across items
@@ -188,26 +190,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             // also completes one o_done[t] phase when its last MMA is done.
             uint32_t q_loads[kTiles] = {0, 0};
             bool ok = true;
+            // A bounded wait polled by the whole warp together, made warp-uniform.
+            auto wwait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+            };
             auto load_kv = [&](int j, int which, int bh) {
                 const int s = it % kStages;
                 const uint32_t use = it / kStages;
-                if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, abort_flag, p.status))
+                if (use > 0 && !wwait(&bars->kv_empty[s], (use - 1) & 1))
                     return false;
-                fa_check(j * kBlockN < p.sc.Sk && bh < p.sc.BH, p.status);
-                mbar_arrive_expect_tx(&bars->kv_full[s], kTileBytes);
-                tma_load_3d_hint(sKV + s * kTileBytes, which == 0 ? &tm_k : &tm_v,
-                                 &bars->kv_full[s], 0, j * kBlockN, bh, pol_keep);
+                if (lane == 0) {
+                    fa_check(j * kBlockN < p.sc.Sk && bh < p.sc.BH, p.status);
+                    mbar_arrive_expect_tx(&bars->kv_full[s], kTileBytes);
+                    tma_load_3d_hint(sKV + s * kTileBytes, which == 0 ? &tm_k : &tm_v,
+                                     &bars->kv_full[s], 0, j * kBlockN, bh, pol_keep);
+                }
+                __syncwarp();
                 ++it;
                 return true;
             };
             for (int n = 0; ok; ++n) {
                 const int slot = n % kQueue;
-                if (n >= kQueue &&
-                    !mbar_wait(&bars->item_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status))
+                if (n >= kQueue && !wwait(&bars->item_empty[slot], ((n / kQueue) - 1) & 1))
                     break;
-                const int w = sched::grab_item(p.sc);
-                bars->items[slot] = w;
-                mbar_arrive(&bars->item_full[slot]);  // release: the consumers read items[slot]
+                int w = 0;
+                if (lane == 0) {
+                    w = sched::grab_item(p.sc);
+                    bars->items[slot] = w;
+                    mbar_arrive(&bars->item_full[slot]);  // release: the consumers read items[slot]
+                }
+                w = __shfl_sync(0xffffffffu, w, 0);
                 if (w < 0)
                     break;
                 const Item I = sched::decode_item(w, p.sc);
@@ -220,26 +232,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     // Q_t's buffer is free once the previous item's last MMA on
                     // tile t has completed.
-                    if (q_loads[t] > 0 &&
-                        !mbar_wait(&bars->o_done[t], (q_loads[t] - 1) & 1, abort_flag, p.status)) {
+                    if (q_loads[t] > 0 && !wwait(&bars->o_done[t], (q_loads[t] - 1) & 1)) {
                         ok = false;
                         break;
                     }
-                    fa_check(I.q0[t] < p.sc.Sq && I.bh < p.sc.BH, p.status);
-                    mbar_arrive_expect_tx(&bars->q_full[t], kTileBytes);
-                    tma_load_3d_hint(sQ + t * kTileBytes, &tm_q, &bars->q_full[t], 0, I.q0[t],
-                                     p.zero_q ? p.sc.BH : I.bh, pol_stream);
+                    if (lane == 0) {
+                        fa_check(I.q0[t] < p.sc.Sq && I.bh < p.sc.BH, p.status);
+                        mbar_arrive_expect_tx(&bars->q_full[t], kTileBytes);
+                        tma_load_3d_hint(sQ + t * kTileBytes, &tm_q, &bars->q_full[t], 0, I.q0[t],
+                                         p.zero_q ? p.sc.BH : I.bh, pol_stream);
+                    }
+                    __syncwarp();
                     ++q_loads[t];
                 }
                 for (int j = 1; j < I.n_kv_max && ok; ++j)
                     ok = load_kv(j, 0, I.bh) && load_kv(j, 1, I.bh);
             }
             // Drain: every load issued must have landed before the CTA exits.
-            for (int t = 0; t < kTiles; ++t)
-                if (q_loads[t] > 0)
-                    mbar_wait_drain(&bars->q_full[t], (q_loads[t] - 1) & 1, p.status);
-            for (int k = max(0, it - kStages); k < it; ++k)
-                mbar_wait_drain(&bars->kv_full[k % kStages], (k / kStages) & 1, p.status);
+            if (lane == 0) {
+                for (int t = 0; t < kTiles; ++t)
+                    if (q_loads[t] > 0)
+                        mbar_wait_drain(&bars->q_full[t], (q_loads[t] - 1) & 1, p.status);
+                for (int k = max(0, it - kStages); k < it; ++k)
+                    mbar_wait_drain(&bars->kv_full[k % kStages], (k / kStages) & 1, p.status);
+            }
+            __syncwarp();
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
