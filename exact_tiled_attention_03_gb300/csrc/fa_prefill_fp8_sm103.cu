@@ -13,7 +13,8 @@
 // take work items (two 128-row query tiles of one head, fa_schedule.cuh) from
 // a per-launch counter and pass them to their warps through a shared-memory
 // queue; warp 8 feeds a TMA ring of K/V tiles, warp 9 issues tcgen05.mma
-// (here .kind::f8f6f4, 32 elements of K per instruction), warps 0-3 and 4-7
+// (here .kind::f8f6f4, 32 elements of K per instruction; both warps run their
+// loops as a whole warp, one lane issuing), warps 0-3 and 4-7
 // run the softmax of one tile each with S and O in tensor memory, and the MMA
 // order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) overlaps each tile's softmax
 // with the other's products. What differs:
@@ -262,8 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         // Per item, ring order K_0, V_0, K_1, V_1, ...; issue order S_0(0),
         // S_1(0), then per j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), as in the
-        // bf16 kernel.
-        if (lane == 0) {
+        // bf16 kernel, and like it run by the whole warp: the warp polls each
+        // barrier together, and one elected lane issues each MMA and commit.
+        {
             const uint32_t idesc_qk = idesc_e4m3_f32(kBlockM, kBlockN, false, false) | p.idesc_qk_neg;
             constexpr uint32_t idesc_pv = idesc_e4m3_f32(kBlockM, kD, false, true);
             const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
@@ -278,33 +280,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t a0 = dq0 + kTileStep * t, b0 = dk0 + kTileStep * slot;
 #pragma unroll
                 for (int kk = 0; kk < kD / 32; ++kk)
-                    umma_f8_ss(tmem + col_s(t), a0 + 2 * kk, b0 + 2 * kk, idesc_qk, kk > 0 ? 1u : 0u);
+                    umma_f8_ss_elect(tmem + col_s(t), a0 + 2 * kk, b0 + 2 * kk, idesc_qk, kk > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int slot, int j) {
                 const uint64_t b0 = dv0 + kTileStep * slot;
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 32; ++kk)
-                    umma_f8_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8,
+                    umma_f8_ts_elect(tmem + col_o(t), tmem + col_s(t) + kk * 8,
                                b0 + static_cast<uint64_t>((kk * 32 * 128) >> 4), idesc_pv,
                                (j > 0 || kk > 0) ? 1u : 0u);
             };
+            // A bounded wait polled by the whole warp together, made warp-uniform.
+            auto wwait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+            };
             auto ring_wait = [&](int idx) {
-                return mbar_wait(&bars->kv_full[idx % kStages], (idx / kStages) & 1, abort_flag,
-                                 p.status);
+                return wwait(&bars->kv_full[idx % kStages], (idx / kStages) & 1);
             };
             int it = 0;
             uint32_t q_waits[kTiles] = {0, 0}, p_waits[kTiles] = {0, 0};
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 const int slot = n % kQueue;
-                if (!mbar_wait(&bars->item_full[slot], (n / kQueue) & 1, abort_flag, p.status))
+                if (!wwait(&bars->item_full[slot], (n / kQueue) & 1))
                     break;
-                const int w = bars->items[slot];
+                const int w = __shfl_sync(0xffffffffu, lane == 0 ? bars->items[slot] : 0, 0);
                 if (w < 0)
                     break;
                 const Item I = sched::decode_item(w, p.sc);
                 if (I.n_kv_max == 0) {
-                    mbar_arrive(&bars->item_empty[slot]);
+                    if (lane == 0)
+                        mbar_arrive(&bars->item_empty[slot]);
                     continue;
                 }
                 // S_t(0) as soon as Q_t is in.
@@ -312,16 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < kTiles && ok; ++t) {
                     if (I.n_kv[t] == 0)
                         continue;
-                    ok = mbar_wait(&bars->q_full[t], (q_waits[t]++) & 1, abort_flag, p.status);
+                    ok = wwait(&bars->q_full[t], (q_waits[t]++) & 1);
                     if (!ok)
                         break;
                     tc_fence_after_sync();
                     issue_s(t, it % kStages);
-                    umma_commit(&bars->s_full[t]);
+                    umma_commit_elect(&bars->s_full[t]);
                 }
                 if (!ok)
                     break;
-                umma_commit(&bars->kv_empty[it % kStages]);
+                umma_commit_elect(&bars->kv_empty[it % kStages]);
                 for (int j = 0; j < I.n_kv_max && ok; ++j) {
                     const int iv = it + 2 * j + 1, ik = it + 2 * j + 2;
                     ok = ring_wait(iv);  // V_j
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < kTiles && ok; ++t) {
                         if (j >= I.n_kv[t])
                             continue;
-                        ok = mbar_wait(&bars->p_full[t], (p_waits[t]++) & 1, abort_flag, p.status);
+                        ok = wwait(&bars->p_full[t], (p_waits[t]++) & 1);
                         if (!ok)
                             break;
                         tc_fence_after_sync();
@@ -346,23 +352,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 k_ready = true;
                             }
                             issue_s(t, ik % kStages);
-                            umma_commit(&bars->s_full[t]);
+                            umma_commit_elect(&bars->s_full[t]);
                         } else {
-                            umma_commit(&bars->o_done[t]);  // this tile's last PV of the item
+                            umma_commit_elect(&bars->o_done[t]);  // this tile's last PV of the item
                         }
                     }
                     if (!ok)
                         break;
-                    umma_commit(&bars->kv_empty[iv % kStages]);
+                    umma_commit_elect(&bars->kv_empty[iv % kStages]);
                     if (k_ready)
-                        umma_commit(&bars->kv_empty[ik % kStages]);
+                        umma_commit_elect(&bars->kv_empty[ik % kStages]);
                 }
                 it += 2 * I.n_kv_max;
-                mbar_arrive(&bars->item_empty[slot]);  // every MMA of the item is issued
+                if (lane == 0)
+                    mbar_arrive(&bars->item_empty[slot]);  // every MMA of the item is issued
             }
-            // Drain: all MMAs issued by this thread complete before TMEM is freed.
-            umma_commit(&bars->drain);
-            mbar_wait_drain(&bars->drain, 0, p.status);
+            // Drain: all MMAs issued by the elected lane complete before TMEM is freed.
+            umma_commit_elect(&bars->drain);
+            if (lane == 0)
+                mbar_wait_drain(&bars->drain, 0, p.status);
+            __syncwarp();
         }
     } else if (warp < kSoftmaxWarps) {
         // ------------------------------------------------------------ softmax warpgroups
