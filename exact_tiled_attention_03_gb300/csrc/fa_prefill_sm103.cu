@@ -141,6 +141,46 @@ using sched::visible_keys;
 static_assert(kTiles == sched::kTiles && kBlockM == sched::kTileRows && kBlockN == sched::kKeyTile,
               "the kernel's tiles are the schedule's items");
 
+// 64 TMEM columns of this thread's lane, without waiting: the registers are
+// written when the load completes, which tmem_ld_wait_regs64 waits for.
+__device__ __forceinline__ void tmem_ld64_nowait(uint32_t taddr, uint32_t (&r)[64])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]),
+          "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]),
+          "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]),
+          "=r"(r[63])
+        : "r"(taddr), "r"(taddr + 32u)
+        : "memory");
+}
+
+// Wait for this thread's TMEM loads; r is an operand (read and written), so
+// every use of the loaded registers stays after the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs64(uint32_t (&r)[64])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]),
+                   "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]),
+                   "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]),
+                   "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
+                   "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]),
+                   "+r"(r[63])
+                 :
+                 : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -705,16 +745,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = (ln > 0.0f) ? 1.0f / ln : 0.0f;
             uint8_t *sOut = smem + C::kOffOut + t * kBoxBytes;
             const uint32_t sOut_a = smem_u32(sOut);
+            // Box b (O's columns 64 b .. 64 b + 63) is in the staging box: send it.
+            auto store_box = [&](int b) {
+                fence_proxy_async_smem();
+                named_bar_sync(1 + t, 128);
+                if (r == 0) {
+                    fa_check(q0 < p.sc.Sq && I.bh < p.sc.BH, p.status);
+                    tma_store_3d(&tm_o, sOut, b * 64, q0, I.bh);
+                    tma_store_commit();
+                    // The next box is written only after this store has read the
+                    // box (the barrier at the top of the next box); at d = 128
+                    // the last box's read is waited for at the next epilogue.
+                    // The writes to global memory finish on their own.
+                    if (b + 1 < C::kBoxes || !kDeferLastRead)
+                        tma_store_wait_read_all();
+                }
+            };
+            if constexpr (D == 128) {
+                // The second box's TMEM load is issued as soon as the first box
+                // is in shared memory and waited for after the barrier, so its
+                // latency overlaps the first box's store (0.99x the headline's
+                // time against loading it after that barrier; at d = 64, one
+                // box, a single 64-column load measured 1.017x, so d = 64 keeps
+                // two 32-column loads below).
+                uint32_t o[64];
+                if (n_kv > 0) {
+                    tmem_ld64_wait(tO, o);
+                } else {
 #pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b) {
-                if (b > 0)
-                    named_bar_sync(1 + t, 128);  // the previous box has been read out
+                    for (int c = 0; c < 64; ++c)
+                        o[c] = 0u;
+                }
+#pragma unroll
+                for (int b = 0; b < C::kBoxes; ++b) {
+                    if (b > 0) {
+                        named_bar_sync(1 + t, 128);  // the previous box has been read out
+                        if (n_kv > 0)
+                            tmem_ld_wait_regs64(o);
+                    }
+                    uint32_t pko[32];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2)
+                        pko[c / 2] = pack_bf16x2(__uint_as_float(o[c]) * inv_l,
+                                                 __uint_as_float(o[c + 1]) * inv_l);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(sOut_a + sw128_offset(static_cast<uint32_t>(r), static_cast<uint32_t>(q)),
+                                     pko[4 * q], pko[4 * q + 1], pko[4 * q + 2], pko[4 * q + 3]);
+                    if (b + 1 < C::kBoxes && n_kv > 0)
+                        tmem_ld64_nowait(tO + 64 * (b + 1), o);
+                    store_box(b);
+                }
+            } else {
 #pragma unroll
                 for (int c1 = 0; c1 < 64; c1 += 32) {
-                    const int c0 = 64 * b + c1;
                     uint32_t o[32];
                     if (n_kv > 0) {
-                        tmem_ld32_wait(tO + c0, o);
+                        tmem_ld32_wait(tO + c1, o);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
@@ -732,19 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      pko[q * 4], pko[q * 4 + 1], pko[q * 4 + 2], pko[q * 4 + 3]);
                     }
                 }
-                fence_proxy_async_smem();
-                named_bar_sync(1 + t, 128);
-                if (r == 0) {
-                    fa_check(q0 < p.sc.Sq && I.bh < p.sc.BH, p.status);
-                    tma_store_3d(&tm_o, sOut, b * 64, q0, I.bh);
-                    tma_store_commit();
-                    // The next box is written only after this store has read the
-                    // box (the barrier at the top of the next box); at d = 128
-                    // the last box's read is waited for at the next epilogue.
-                    // The writes to global memory finish on their own.
-                    if (b + 1 < C::kBoxes || !kDeferLastRead)
-                        tma_store_wait_read_all();
-                }
+                store_box(0);
             }
             if (i < p.sc.Sq) {
                 // ref is in log2 units: ref * ln 2 is the max in units of the
