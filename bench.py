@@ -26,6 +26,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -55,10 +56,14 @@ def dist_env():
     return world, rank, local
 
 
-def init_dist(world, backend):
+def init_dist(world, backend, timeout_s: float = 600.0):
+    """One process group for the job. A rank that dies ends the others' next
+    collective with an error within `timeout_s` (or at once, when its
+    connections close) instead of the backend's default wait."""
     if world > 1 and not torch.distributed.is_initialized():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        torch.distributed.init_process_group(backend=backend)
+        torch.distributed.init_process_group(backend=backend,
+                                             timeout=datetime.timedelta(seconds=timeout_s))
 
 
 def barrier(world):

@@ -97,6 +97,42 @@ def _run(fn, world=2):
     return dict(out)
 
 
+def _dead_rank(rank, world, port, out):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    os.environ["RANK"] = str(rank)
+    os.environ["WORLD_SIZE"] = str(world)
+    import bench
+
+    bench.init_dist(world, "gloo", timeout_s=20.0)
+    if rank == 1:
+        os._exit(3)  # fails between steps, before the timing reduction
+    try:
+        bench.reduce_max(1.0, world)
+        out[rank] = "no error"
+    except Exception as e:  # the backend's error type differs across versions
+        out[rank] = "error: " + type(e).__name__
+
+
+def test_a_dead_rank_ends_the_others_reduction_with_an_error():
+    """A rank that exits between steps makes the survivor's next collective
+    raise (bounded by the process-group timeout) rather than wait for it."""
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_dead_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert procs[1].exitcode == 3
+    assert procs[0].exitcode == 0, procs[0].exitcode
+    assert out.get(0, "").startswith("error"), dict(out)
+
+
 def test_bench_rank_logic_two_gloo_ranks():
     out = _run(_bench_logic)
     seeds, t_max, work, per_rank = out[0]
