@@ -69,9 +69,12 @@ constexpr int kBoxBytes = kBlockM * 128;  // one 128-row x 64-column bf16 box (1
 // Lazy rescale threshold, in log2 units of the exponent (factor 256).
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kRescaleFactor = 256.0f;  // 2^kRescaleLog2
-// d = 128: largest row sum settled by shifting the p already computed (below it
-// no p can have overflowed, and 2^100 stays far inside fp32 and bf16 range); a
-// larger sum recomputes against the exact max.
+// d = 128: a row sum above 2^kRescaleLog2 but at most kMoveLimit leaves the
+// reference where it is (every p of the tile is then at most 2^16, far inside
+// bf16 and fp32 range). Up to kShiftLimit the reference moves by shifting the p
+// already computed (below it no p can have overflowed); a larger sum
+// recomputes against the exact max.
+constexpr float kMoveLimit = 0x1p16f;
 constexpr float kShiftLimit = 0x1p100f;
 
 template <int D>
@@ -498,16 +501,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ref: the reference of this row's exponentials, in log2 units of
             // the exponent (p = 2^(s * sl2 - ref), s the MMA's score). It is
-            // set by the row's first visible tile to that tile's max and moved
-            // only when a tile's p would exceed 2^kRescaleLog2: by an integer
-            // k, multiplying the p already computed (bf16) and O, l by 2^-k,
-            // all exact. O and l always share the reference, so the result
-            // stays exact, and P stays <= 2^kRescaleLog2.
+            // set by the row's first visible tile to that tile's max. At d = 128
+            // it moves only when a row sum of p against it exceeds kMoveLimit
+            // (so P stays <= 2^16): by an integer k, multiplying the p already
+            // computed (bf16) and O, l by 2^-k, all exact. At d = 64 it moves
+            // when a tile's max lies more than 2^kRescaleLog2 above it (P stays
+            // <= 2^kRescaleLog2). O and l always share the reference, so the
+            // result stays exact.
             float ref = -INFINITY;
             float l = 0.0f;  // running sum of 2^(s * sl2 - ref), fp32 (for the LSE)
-            // O's divisor: l, except that a tile whose reference moved in place
-            // adds the sum of its bf16 weights (those P V used), so that a row's
-            // dominant weight, rounded to bf16 there, cancels in O / ln.
+            // O's divisor: l, except that at d = 128 a tile with a row sum above
+            // 2^kRescaleLog2 adds the sum of its bf16 weights (those P V used),
+            // so that a row's dominant weight, rounded to bf16 there, cancels in
+            // O / ln.
             float ln = 0.0f;
             for (int j = 0; j < n_kv && ok; ++j) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], (s_waits++) & 1,
@@ -615,8 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc[q] = fmul2(acc[q], fx2);
                     ref_use = ref + static_cast<float>(k);
                     corr = f;
-                    if (k > 0)
-                        norm_sum = sum_bf16x2_row(pk);
                 };
                 // O_t *= corr after a move (warp-uniform; lanes that did not move
                 // multiply by 1). PV_t(j-1) has completed: S_t(j), committed after
@@ -654,12 +658,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Speculative pass without the max: when every lane has a
                     // reference, p is computed against it. Every p is >= 0, so a row
                     // sum of at most 2^kRescaleLog2 shows that no p exceeds
-                    // 2^kRescaleLog2 and the reference stays. A larger sum (up to
-                    // kShiftLimit, so that no p can have overflowed) is settled
-                    // from the packed p: their max, and a shift by its exponent when
-                    // it exceeds 2^kRescaleLog2. Only a larger sum, or a row's first
-                    // tile, runs the max pass and then the exponentials against the
-                    // new reference. The passes run one per iteration of this loop,
+                    // 2^kRescaleLog2 and the reference stays. When every row sum
+                    // is at most kMoveLimit the reference stays too, and O's
+                    // divisor takes the tile's bf16 weights (those P V uses): a
+                    // weight that dominates its row is then the same in O and in
+                    // its divisor. A larger sum (up to kShiftLimit, so that no p
+                    // can have overflowed) is settled from the packed p: their
+                    // max, and a shift by its exponent when it exceeds
+                    // 2^kRescaleLog2. Only a larger sum, or a row's first tile,
+                    // runs the max pass and then the exponentials against the new
+                    // reference. The passes run one per iteration of this loop,
                     // so the code holds one copy of the pass (three copies spilled
                     // at 168 registers). Stages: 0 speculative exponentials, 1 max,
                     // 2 exponentials.
@@ -676,13 +684,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!__any_sync(0xffffffffu, sum > kRescaleFactor))
                                 break;
                             if (__all_sync(0xffffffffu, sum <= kShiftLimit)) {
-                                const float pmax = max_bf16x2_row(pk);
-                                const int k =
-                                    pmax > kRescaleFactor ? (__float_as_int(pmax) >> 23) - 127 : 0;
-                                any_move = __any_sync(0xffffffffu, k > 0);
-                                if (any_move) {
-                                    shift(k);
-                                    rescale_o();
+                                // Up to kMoveLimit the reference stays (0.84x the
+                                // time of shifting by the max's exponent on the 2K
+                                // Q x 4 input: no multiply of P, no TMEM round trip
+                                // of O). A sum above it implies a p above 2^9, so
+                                // some lane moves.
+                                // O's divisor takes the bf16 weights (summed below
+                                // the loop where norm_sum is set to 0): every lane's
+                                // when the reference stays, the moved lanes' after a
+                                // move.
+                                norm_sum = 0.0f;
+                                if (!__all_sync(0xffffffffu, sum <= kMoveLimit)) {
+                                    const float pmax = max_bf16x2_row(pk);
+                                    const int k =
+                                        pmax > kRescaleFactor ? (__float_as_int(pmax) >> 23) - 127 : 0;
+                                    norm_sum = k > 0 ? 0.0f : -1.0f;
+                                    any_move = __any_sync(0xffffffffu, k > 0);
+                                    if (any_move) {
+                                        shift(k);
+                                        rescale_o();
+                                    }
                                 }
                                 break;
                             }
@@ -695,6 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                     }
+                    if (norm_sum == 0.0f)
+                        norm_sum = sum_bf16x2_row(pk);
                 } else {
                     // d = 64: the speculative pass finds the tile's max while it
                     // computes p against the reference (the form above measured

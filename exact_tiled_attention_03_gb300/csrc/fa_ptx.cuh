@@ -674,17 +674,35 @@ __device__ __forceinline__ float max_bf16x2_row(const uint32_t (&v)[N])
     return fmaxf(__uint_as_float(t[0] << 16), __uint_as_float(t[0] & 0xFFFF0000u));
 }
 
-// Sum of the 2 * N bf16 values packed in v, in fp32.
+// x + (bf16) h for the low (H = 0) or high (H = 1) half of the pair v: one
+// mixed-precision add (the bf16 operand widens exactly, the sum rounds once).
+template <int H>
+__device__ __forceinline__ float add_f32_bf16(float x, uint32_t v)
+{
+    float d;
+    if constexpr (H == 0)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+            "add.rn.f32.bf16 %0, lo, %2;\n\t}" : "=f"(d) : "r"(v), "f"(x));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+            "add.rn.f32.bf16 %0, hi, %2;\n\t}" : "=f"(d) : "r"(v), "f"(x));
+    return d;
+}
+
+// Sum of the 2 * N bf16 values packed in v, in fp32: eight chains (element
+// 2i into chain 2 (i % 4), element 2i + 1 into chain 2 (i % 4) + 1), then a
+// fixed tree. Mixed-precision adds take each half straight from its pair.
 template <int N>
 __device__ __forceinline__ float sum_bf16x2_row(const uint32_t (&v)[N])
 {
-    float2 a[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                   make_float2(0.f, 0.f)};
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < N; ++i)
-        a[i % 4] = fadd2(a[i % 4], make_float2(__uint_as_float(v[i] << 16),
-                                               __uint_as_float(v[i] & 0xFFFF0000u)));
-    const float2 t = fadd2(fadd2(a[0], a[1]), fadd2(a[2], a[3]));
+    for (int i = 0; i < N; ++i) {
+        a[2 * (i % 4)] = add_f32_bf16<0>(a[2 * (i % 4)], v[i]);
+        a[2 * (i % 4) + 1] = add_f32_bf16<1>(a[2 * (i % 4) + 1], v[i]);
+    }
+    const float2 t = fadd2(fadd2(make_float2(a[0], a[1]), make_float2(a[2], a[3])),
+                           fadd2(make_float2(a[4], a[5]), make_float2(a[6], a[7])));
     return t.x + t.y;
 }
 

@@ -167,6 +167,37 @@ def test_prefill_large_logits_rescale():
     compare(o, lse, ro, rl)
 
 
+def test_prefill_dominant_key_on_a_later_tile():
+    """Key 300 (the third key tile) outweighs the rest of every row that sees it
+    by about 2^11, and its V row is +-7.875. That tile's row sums lie between
+    2^8 and 2^16, so the d = 128 kernel keeps the reference and divides O by the
+    sum of the bf16 weights P V used: O is then within half a bf16 ulp of the
+    exact result plus 8e-3. Dividing by the fp32 sum instead leaves the dominant
+    weight's bf16 rounding (up to 2^-9 of |v|) in O: 2.8e-2 beyond half an ulp
+    in a CPU model of the kernel's arithmetic. |O| near 7.6 puts the bf16
+    output's own rounding at up to 1.56e-2, hence the per-element bound."""
+    g = torch.Generator().manual_seed(7)
+    B, H, S, d = 1, 2, 640, 128
+    q = torch.randn(B, H, S, d, generator=g) * 0.25
+    q[..., 0] = 8.0
+    k = torch.randn(B, H, S, d, generator=g)
+    v = torch.randn(B, H, S, d, generator=g)
+    k[:, :, 300, 0] = 13.25
+    v[:, :, 300, :] = torch.where(torch.arange(d) % 2 == 0, 7.875, -7.875)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run("fa_prefill_forward", q, k, v, True, scale)
+    ro, rl = oracle_full(q, k, v, True, scale)
+    og = np.asarray(o, dtype=np.float64)
+    ro = np.asarray(ro, dtype=np.float64).reshape(og.shape)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ro), 2.0**-126))) - 8)
+    excess = np.abs(og - ro) - half_ulp
+    assert excess.max() <= 8e-3, excess.max()
+    assert np.abs(ro[0, :, 300:]).max() > 7.0  # the dominant key decides the rows that see it
+    lg = np.asarray(lse, dtype=np.float64)
+    assert np.abs(lg - np.asarray(rl, dtype=np.float64).reshape(lg.shape)).max() <= 1e-3
+
+
 def test_prefill_matches_simt_reference():
     w = custom(2, 2, 384, 512, 128, True, seed=5)
     q, k, v = make_qkv(w)
