@@ -291,7 +291,11 @@ size_t fa_backward_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
  * The (b, h) pairs are processed in FA_HOST_CHUNKS consecutive groups: the
  * host-to-device copies of group c+1 overlap the kernels of group c and the
  * device-to-host copies of group c-1, on copy and compute streams owned by
- * the library. All of it is ordered after work already queued on `stream`,
+ * the library. When o is pinned host memory mapped into the device's address
+ * space (cudaHostAlloc / cudaHostRegister under unified addressing) and
+ * 16-byte aligned, O returns through stores by a few CTAs of the library,
+ * which leave the host link to the input copies; otherwise, and for lse,
+ * through cudaMemcpyAsync. All of it is ordered after work already queued on `stream`,
  * and `stream` waits for all of it, so synchronising `stream` (or an event
  * recorded on it afterwards) means o and lse are filled. Calls from several
  * host threads are serialised on the library's streams.

@@ -372,6 +372,34 @@ def test_forward_host_buffers(case, pinned, own_workspace):
     compare(o.float(), lse, ro, rl)
 
 
+def test_forward_host_output_paths_agree_bit_for_bit():
+    """O returns through stores by a few CTAs into a pinned, 16-byte aligned host
+    buffer, and through cudaMemcpyAsync into a pageable or unaligned one: the
+    bytes are the same."""
+    B, H, S, d = 2, 4, 640, 128
+    w = custom(B, H, S, S, d, True, seed=5)
+    q, k, v = (t.pin_memory() for t in make_qkv(w))
+    n = q.numel()
+    outs = []
+    for kind in ("pinned", "pageable", "pinned_unaligned"):
+        if kind == "pinned":
+            o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, pin_memory=True)
+        elif kind == "pageable":
+            o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16)
+        else:
+            base = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, pin_memory=True)
+            o = base[1:1 + n].view(q.shape)  # 2 bytes past a 16-byte boundary
+        lse = torch.full((B, H, S), float("nan"), dtype=torch.float32)
+        _capi.check(_capi.fa_forward_host(q, k, v, o, lse, B, H, S, S, d, True, w.scale, None, 0),
+                    "fa_forward_host")
+        torch.cuda.current_stream().synchronize()
+        _capi.check(_capi.fa_device_status(), "device status")
+        outs.append((o.clone(), lse.clone()))
+    assert torch.isfinite(outs[0][0].float()).all()
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
 def test_forward_host_rejects_a_small_workspace():
     w = custom(1, 2, 300, 300, 128, True)
     q, k, v = make_qkv(w)
