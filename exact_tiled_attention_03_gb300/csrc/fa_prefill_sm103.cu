@@ -33,10 +33,13 @@
 //     chunks, masks, and computes exp2 of the log2(e)-scaled logits against
 //     its current reference max (at d = 64 while it finds the tile's max; at
 //     d = 128 without it, the row sum of those exponentials showing whether
-//     any exceeds 2^8); only if the tile's max exceeds the reference by more
-//     than 2^8 (or on the row's first tile) does it recompute the row against
-//     the new max and rescale its O row in TMEM. It then writes P (bf16) over
-//     its S row in TMEM. At the end
+//     any exceeds 2^8). At d = 64 a tile whose max exceeds the reference by
+//     more than 2^8 (or a row's first tile) is recomputed against the new max
+//     and the O row rescaled in TMEM. At d = 128 a row sum above 2^8 adds the
+//     tile's bf16 weights to O's divisor, and only a sum above 2^16 moves the
+//     reference, by a power of two that scales P and O exactly; a row's first
+//     tile, or a sum above 2^100, is recomputed against the max. It then
+//     writes P (bf16) over its S row in TMEM. At the end
 //     of an item it divides by l and writes its bf16 O row into the tile's
 //     own staging box in shared memory, 64 columns at a time, each box sent
 //     by one TMA store; then it writes its LSE. Q's buffers are reloaded for
@@ -580,12 +583,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     return mx;
                 };
-                // The reference max m moves only when the tile's max exceeds it by
-                // more than 2^kRescaleLog2 (or on the first visible key); O and l
-                // always share it, so the result stays exact and P stays <=
-                // 2^kRescaleLog2. NaN (both -inf) compares false: nothing visible
-                // yet, keep m. Until P is written, S_t is intact and may be read
-                // again.
+                // On the max-based path (d = 64, and d = 128's first tiles and
+                // recomputations) the reference moves only when the tile's max
+                // exceeds it by more than 2^kRescaleLog2 (or on the first visible
+                // key), so that tile's P stays <= 2^kRescaleLog2; O and l always
+                // share the reference, so the result stays exact. NaN (both -inf)
+                // compares false: nothing visible yet, keep the reference. Until
+                // P is written, S_t is intact and may be read again.
                 float ref_use = ref, corr = 1.0f;
                 bool any_move = false;  // some lane of the warp moved its reference
                 float norm_sum = -1.0f;  // >= 0: this tile's contribution to ln (else the fp32 sum)
